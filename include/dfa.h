@@ -1,0 +1,263 @@
+/*
+ * dfa.h -- C ABI of libdfa: exact causal blockwise attention (forward and
+ * recomputation backward), chunk-pair partials, log-sum-exp merge, sequence
+ * permutes and ring schedules, for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Tensors are row-major [B, H, L, d] (batch, head, token, feature),
+ *   contiguous, on the device, 16-byte aligned.  Q, K, V, O, dO, dQ, dK, dV
+ *   are bf16 unless a call says fp32.  LSE and D are fp32 [B, H, L].
+ * - d (head dimension) is 64 or 128.  Hq % Hkv == 0; query head h reads
+ *   key/value head h / (Hq / Hkv) (grouped-query attention).
+ * - LSE is the natural-log log-sum-exp of the scaled, masked scores of a row:
+ *   LSE_i = ln sum_j exp(scale * q_i . k_j).  A row that sees no key has
+ *   LSE = -inf and O = 0.
+ * - Causal masking is by global token position: key j is visible to query i
+ *   iff pos(j) <= pos(i) (the diagonal is visible).
+ * - Every call is asynchronous on the caller's CUDA stream (passed as void*,
+ *   a cudaStream_t; NULL = legacy default stream).  No call allocates device
+ *   memory or synchronises the device, except dfa_stream_status, which
+ *   synchronises the given stream.  The caller owns every buffer; the library
+ *   keeps no pointer after a call returns.
+ * - Errors: argument errors are reported synchronously through the return
+ *   value (no work is launched); launch failures return DFA_ERR_CUDA; a
+ *   device-side wait that exceeds its time limit sets a status word in the
+ *   workspace, read back by dfa_stream_status (DFA_ERR_TIMEOUT).  The text
+ *   of the last error of the calling thread is in dfa_last_error().
+ * - Workspace: calls that take (ws, ws_bytes) need at least
+ *   dfa_workspace_size(desc, op) bytes, 256-byte aligned, whose first 256
+ *   bytes (the status word) the caller zeroes once when allocating it.
+ *   Workspace contents other than the status word are scratch.
+ *
+ * Sources of the method (web pages):
+ * - "Striped Attention Guide: Faster Causal Ring Attention": "The Fatal Flaw:
+ *   Causal Workload Imbalance" (causal score matrix), "Incremental Online
+ *   Softmax Rescaling" (running max, sum, rescale of partial states),
+ *   "Intra-Block vs. Inter-Block Masking Logic" (full / diagonal / skipped
+ *   tiles), "Mathematical Formulation of Token Striping" and "Workload
+ *   Balance Theorem" (striped partition, ring steps).
+ * - "DistFlashAttn Guide: Distributed Attention for Long LLMs": "The Folded
+ *   Chunk Assignment" (load-balanced partition), "The Causal Imbalance
+ *   Crisis" (contiguous ring bubble and eta_util).
+ * - "FlashAttention" glossary entry: tiled exact attention, O(N) memory, the
+ *   backward pass recomputed from per-row softmax statistics.
+ */
+#ifndef DFA_H
+#define DFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dfa_status {
+    DFA_OK = 0,
+    DFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shape   */
+    DFA_ERR_UNSUPPORTED = 2, /* valid but not implemented (d, alignment, map) */
+    DFA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
+    DFA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed             */
+    DFA_ERR_TIMEOUT = 5      /* a device-side wait gave up (async, see above) */
+} dfa_status;
+
+/* Sequence partitions over P logical workers (chunks). */
+enum {
+    DFA_PART_CONTIGUOUS = 0, /* worker p: tokens [p n, (p+1) n), n = N / P   */
+    DFA_PART_BALANCED = 1,   /* 2P chunks of N/(2P); worker p: chunk p then
+                                chunk 2P-1-p (DistFlashAttn folded)          */
+    DFA_PART_STRIPED = 2     /* blocks of `stripe` tokens dealt round-robin:
+                                worker p owns blocks b with b mod P == p      */
+};
+
+/* Problem descriptor (plain data, caller-owned). */
+typedef struct dfa_attn_desc {
+    int32_t B;         /* batch                                            */
+    int32_t Hq;        /* query heads                                      */
+    int32_t Hkv;       /* key/value heads, Hq % Hkv == 0                   */
+    int64_t N;         /* tokens per sequence                              */
+    int32_t d;         /* head dimension, 64 or 128                        */
+    int32_t causal;    /* 1 causal, 0 full attention                       */
+    float scale;       /* softmax scale, usually 1/sqrt(d)                 */
+    int32_t P;         /* logical workers (chunks), >= 1, N % P == 0        */
+    int32_t partition; /* DFA_PART_*                                       */
+    int32_t stripe;    /* striped block size in tokens (1 = token stripes) */
+    int32_t o_fp32;    /* dfa_attn_fwd output O: 0 bf16, 1 fp32            */
+} dfa_attn_desc;
+
+/*
+ * Global positions of the rows of a chunk.  The chunk's rows form nseg (1 or
+ * 2) segments; local row m' of segment t (m' counted from the segment start)
+ * has position  base[t] + (m' / blk) * blk_stride + (m' % blk).
+ * Positions must increase strictly along the chunk (blk_stride >= blk, and
+ * base[1] above the last position of segment 0).
+ *   contiguous worker p:  nseg 1, base p n, blk 1, blk_stride 1
+ *   folded worker p:      nseg 2, len n/2 each, bases p n/2 and (2P-1-p) n/2
+ *   striped worker p:     nseg 1, base p s, blk s, blk_stride P s
+ */
+typedef struct dfa_pos_map {
+    int32_t nseg;
+    int32_t reserved;
+    int64_t len[2];
+    int64_t base[2];
+    int64_t blk;
+    int64_t blk_stride;
+} dfa_pos_map;
+
+typedef struct dfa_chunk_pair {
+    dfa_pos_map q;  /* positions of the query chunk's rows     */
+    dfa_pos_map kv; /* positions of the key/value chunk's rows */
+} dfa_chunk_pair;
+
+/* Operations for dfa_workspace_size. */
+enum { DFA_OP_FWD = 0, DFA_OP_BWD = 1, DFA_OP_CHUNK_FWD = 2, DFA_OP_CHUNK_BWD = 3 };
+
+/*
+ * dfa_attn_fwd -- attention forward over a whole sequence (FlashAttention
+ * glossary entry; Striped Attention Guide, "Incremental Online Softmax
+ * Rescaling" and "Intra-Block vs. Inter-Block Masking Logic").
+ *
+ * Storage order: q/k/v/o/lse rows are in worker-major order of desc's
+ * partition -- row r = p*n + m holds the token at global position
+ * pos_p(m) (n = N/P).  With P == 1 or DFA_PART_CONTIGUOUS this is natural
+ * order.  dfa_permute converts between natural and worker-major order.
+ * One launch runs every ring step of every worker: worker p's queries meet
+ * the keys of worker (p - s) mod P for s = 0..P-1, fully masked tiles are
+ * skipped, and the per-step partial states are merged on chip by the same
+ * log-sum-exp rescaling that dfa_lse_merge applies in memory.
+ *   q [B,Hq,N,d] bf16, k/v [B,Hkv,N,d] bf16  (inputs)
+ *   o [B,Hq,N,d] bf16 (desc->o_fp32 == 0) or fp32 (== 1), lse [B,Hq,N] fp32
+ *   ws: dfa_workspace_size(desc, DFA_OP_FWD) bytes.
+ */
+dfa_status dfa_attn_fwd(const dfa_attn_desc* desc, const void* q, const void* k,
+                        const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * dfa_attn_bwd -- recomputation backward of dfa_attn_fwd (FlashAttention
+ * glossary entry: scores are recomputed from Q, K and the per-row LSE instead
+ * of stored).  Same storage order as dfa_attn_fwd.  With D_i = dO_i . O_i,
+ * P = exp(scale Q K^T - LSE):  dV = P^T dO,  dS = P o (dO V^T - D),
+ * dQ = scale dS K,  dK = scale dS^T Q  (dK, dV summed over the Hq/Hkv query
+ * heads of a key/value head).
+ *   o [B,Hq,N,d] bf16 (the forward output), dout [B,Hq,N,d] bf16,
+ *   lse [B,Hq,N] fp32 (the forward's);  dq [B,Hq,N,d], dk/dv [B,Hkv,N,d] bf16.
+ *   ws: dfa_workspace_size(desc, DFA_OP_BWD) bytes (fp32 dQ accumulator and D).
+ */
+dfa_status dfa_attn_bwd(const dfa_attn_desc* desc, const void* q, const void* k,
+                        const void* v, const void* o, const void* dout, const float* lse,
+                        void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * dfa_chunk_fwd -- one chunk pair: a query chunk against a key/value chunk at
+ * the global positions given by pair (Striped Attention Guide, "Incremental
+ * Online Softmax Rescaling", steps 1-2: scores of the local queries against
+ * the current key block, masked where GlobalPos(q) < GlobalPos(k)).
+ * Produces the normalised partial of that pair: o_part = softmax over the
+ * pair's visible keys times V, lse_part its log-sum-exp; rows that see no key
+ * of the chunk get (0, -inf).  desc supplies B, Hq, Hkv, d, causal, scale.
+ *   q [B,Hq,Lq,d] bf16, k/v [B,Hkv,Lk,d] bf16;
+ *   o_part [B,Hq,Lq,d] fp32, lse_part [B,Hq,Lq] fp32.
+ *   Lq, Lk must equal the total lengths of pair->q and pair->kv.
+ */
+dfa_status dfa_chunk_fwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, int64_t Lq,
+                         int64_t Lk, const void* q, const void* k, const void* v,
+                         float* o_part, float* lse_part, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/*
+ * dfa_chunk_bwd -- gradient contribution of one chunk pair to the attention
+ * over the whole sequence.  lse must be the MERGED (whole-sequence) LSE of the
+ * query rows and delta their D_i = dO_i . O_i with the final O; when delta is
+ * NULL it is computed here from o and dout (o bf16 [B,Hq,Lq,d]).
+ * Accumulates (+=) into fp32 dq_acc [B,Hq,Lq,d], dk_acc / dv_acc
+ * [B,Hkv,Lk,d]; the caller zeroes them before the first pair.  dq_acc and
+ * dk_acc include the softmax scale.
+ */
+dfa_status dfa_chunk_bwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, int64_t Lq,
+                         int64_t Lk, const void* q, const void* k, const void* v,
+                         const void* o, const void* dout, const float* lse,
+                         const float* delta, float* dq_acc, float* dk_acc, float* dv_acc,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dfa_lse_merge -- merge k partial results of the same rows by log-sum-exp
+ * rescaling (Striped Attention Guide, "Incremental Online Softmax
+ * Rescaling", the alpha/beta update written for normalised partials):
+ *   LSE = ln sum_c exp(LSE_c),   O = sum_c exp(LSE_c - LSE) O_c.
+ * A row whose partials are all -inf gives (0, -inf), never NaN.
+ *   o_parts [k][rows][d] fp32, lse_parts [k][rows] fp32 (read only)
+ *   o_out [rows][d] fp32 (out_fp32 = 1) or bf16 (0); lse_out [rows] fp32.
+ *   accumulate = 1: (o_out, lse_out) is itself a partial and is merged in
+ *   (in place; requires out_fp32 = 1).  k >= 1, or k = 0 with accumulate.
+ */
+dfa_status dfa_lse_merge(int64_t rows, int32_t d, int32_t k, const float* o_parts,
+                         const float* lse_parts, void* o_out, float* lse_out,
+                         int32_t out_fp32, int32_t accumulate, void* stream);
+
+/*
+ * dfa_permute -- gather rows between natural order and the worker-major order
+ * of desc's partition (Striped Attention Guide, the partitioner's
+ * stripe/unstripe; DistFlashAttn Guide, "The Folded Chunk Assignment").
+ * in/out are [heads][N][row_elems] with elements of elem_bytes (2 or 4).
+ * inverse = 0: out[h][p n + m] = in[h][pos_p(m)];  inverse = 1: the reverse.
+ * in and out must not overlap.  row_elems * elem_bytes must be a multiple of 4.
+ */
+dfa_status dfa_permute(const dfa_attn_desc* desc, int32_t inverse, const void* in, void* out,
+                       int32_t elem_bytes, int64_t row_elems, int64_t heads, void* stream);
+
+/*
+ * Ring schedule (host only, no device work).  For the P workers of desc's
+ * partition: pair_tokens[p*P + s] = visible causal (query, key) token pairs of
+ * worker p at ring step s, when it holds the keys of worker (p - s) mod P
+ * (Striped Attention Guide, "Workload Balance Theorem"; DistFlashAttn Guide,
+ * "The Causal Imbalance Crisis").  Tiles are tile_m query rows by tile_n key
+ * rows inside each chunk pair; tile_counts[(p*P + s)*3 + c] counts tiles of
+ * class c = 0 skipped, 1 full (no mask), 2 partial (element mask).
+ * eta_slots = non-empty (p, s) slots / P^2 (the pages' eta_util);
+ * eta_flops = total pairs / (P * sum_s max_p pair_tokens) (lockstep
+ * utilisation).  Buffers are caller-owned host arrays of P*P and 3*P*P
+ * int64.
+ */
+typedef struct dfa_schedule {
+    int64_t* pair_tokens;
+    int64_t* tile_counts;
+    int64_t total_pairs;
+    double eta_slots;
+    double eta_flops;
+} dfa_schedule;
+
+dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t tile_n,
+                             dfa_schedule* out);
+
+/* The position map of worker p under desc's partition (host only). */
+dfa_status dfa_partition_map(const dfa_attn_desc* desc, int32_t p, dfa_pos_map* out);
+
+/* Bytes of workspace that op needs for desc (0 on invalid arguments). */
+size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op);
+
+/*
+ * Synchronise stream, then read and clear the device status word in ws.
+ * Returns DFA_OK, DFA_ERR_TIMEOUT (a kernel gave up waiting; its outputs are
+ * invalid) or DFA_ERR_CUDA (the stream reported an error).
+ */
+dfa_status dfa_stream_status(void* ws, void* stream);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing will complete, with a limit of timeout_us microseconds;
+ * the wait gives up, records DFA_ERR_TIMEOUT in ws and the kernel returns.
+ */
+dfa_status dfa_selftest_timeout(void* ws, int64_t timeout_us, void* stream);
+
+const char* dfa_status_string(dfa_status s);
+const char* dfa_last_error(void);
+int32_t dfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFA_H */

@@ -405,7 +405,9 @@ void orc_attn_bwd_q_rows(const void* q, const void* k, const void* v,
  * every query row of the group's G heads are computed from the definition;
  * then, for each selected key j, dV_j = sum_{h,i>=j} P_ij dO_i and
  * dK_j = scale sum_{h,i>=j} dS_ij q_i.  krows[r] is the key index j; outputs
- * are dk[r*d + c], dv[r*d + c].  Cost: O(G * N^2 * d).
+ * are dk[r*d + c], dv[r*d + c].  Statistics are computed only for the query
+ * rows that can see a selected key (i >= min krows).  Cost: O(G * (N - min
+ * krows) * N * d).
  * ------------------------------------------------------------------------- */
 void orc_attn_bwd_kv_rows(const void* q, const void* k, const void* v,
                           const void* dout, int f64, int B, int Hq, int Hkv,
@@ -424,14 +426,20 @@ void orc_attn_bwd_kv_rows(const void* q, const void* k, const void* v,
     double* L = (double*)malloc(sizeof(double) * (size_t)G * N);
     double* RC = (double*)malloc(sizeof(double) * (size_t)G * N);
     int64_t kb = (((int64_t)b * Hkv + hk) * N) * d;
+    /* only query rows i >= min(krows) can see a selected key (causal) */
+    int64_t jmin = N;
+    for (int64_t r = 0; r < nkrows; ++r)
+        if (krows[r] < jmin)
+            jmin = krows[r];
+    int64_t nrow = N - jmin;
 #pragma omp parallel
     {
         double* s = (double*)malloc(sizeof(double) * (size_t)N);
         double* dp = (double*)malloc(sizeof(double) * (size_t)N);
 #pragma omp for schedule(dynamic, 16)
-        for (int64_t gi = 0; gi < (int64_t)G * N; ++gi) {
-            int g = (int)(gi / N);
-            int64_t i = gi % N;
+        for (int64_t gi = 0; gi < (int64_t)G * nrow; ++gi) {
+            int g = (int)(gi / nrow);
+            int64_t i = jmin + gi % nrow;
             int64_t qr = ((((int64_t)b * Hq + hk * G + g) * N) + i) * d;
             double m = -INFINITY;
             for (int64_t j = 0; j <= i; ++j) {
@@ -454,8 +462,8 @@ void orc_attn_bwd_kv_rows(const void* q, const void* k, const void* v,
                 dp[j] = acc;
                 rowc += exp(s[j] - Li) * acc;
             }
-            L[gi] = Li;
-            RC[gi] = rowc;
+            L[(int64_t)g * N + i] = Li;
+            RC[(int64_t)g * N + i] = rowc;
         }
         free(s);
         free(dp);

@@ -1,0 +1,142 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+validates arguments (no device work), and its host-side partition maps and ring
+schedules are bit-exact against the oracle's brute-force restatement."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from long_context_flashattention_gb300 import dfa
+
+
+@pytest.fixture(scope="module")
+def L():
+    return dfa.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    declared = dfa.header_symbols()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(L, name), name
+    for name in ["dfa_attn_fwd", "dfa_attn_bwd", "dfa_chunk_fwd", "dfa_chunk_bwd",
+                 "dfa_lse_merge", "dfa_make_schedule"]:
+        assert name in declared
+
+
+def test_status_strings(L):
+    assert L.dfa_status_string(0) == b"ok"
+    assert b"timed out" in L.dfa_status_string(5)
+    assert L.dfa_version() >= 1
+
+
+def test_workspace_sizes():
+    d = dfa.make_desc(1, 32, 32, 131072, 128, P=8, partition="striped")
+    assert dfa.workspace_size(d, dfa.OP_FWD) == 256
+    need = 256 + 32 * 131072 * 128 * 4 + 32 * 131072 * 4
+    assert dfa.workspace_size(d, dfa.OP_BWD) == need
+    bad = dfa.make_desc(1, 32, 32, 1000, 128, P=3)
+    assert dfa.workspace_size(bad, dfa.OP_FWD) == 0
+
+
+def _fwd_code(L, desc, ws_bytes=256, null_q=False):
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) & ~255
+    p = ctypes.c_void_p(base)
+    return L.dfa_attn_fwd(ctypes.byref(desc), None if null_q else p, p, p, p, p, p, ws_bytes,
+                          None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=1, Hq=3, Hkv=2, N=256, d=64), 1),          # Hq % Hkv
+    (dict(B=1, Hq=1, Hkv=1, N=256, d=96), 2),          # head dim
+    (dict(B=1, Hq=1, Hkv=1, N=256, d=64, P=3), 1),     # N % P
+    (dict(B=1, Hq=1, Hkv=1, N=256, d=64, P=64), 2),    # too many chunks
+    (dict(B=1, Hq=1, Hkv=1, N=260, d=64, P=4, partition="balanced"), 1),  # N % 2P
+    (dict(B=0, Hq=1, Hkv=1, N=256, d=64), 1),
+])
+def test_argument_validation(L, kw, code):
+    desc = dfa.make_desc(**kw)
+    assert _fwd_code(L, desc) == code
+    assert L.dfa_last_error()
+
+
+def test_null_pointer_and_workspace(L):
+    desc = dfa.make_desc(1, 1, 1, 256, 64)
+    assert _fwd_code(L, desc, null_q=True) == 1
+    assert _fwd_code(L, desc, ws_bytes=16) == 3
+
+
+def test_merge_validation(L):
+    assert L.dfa_lse_merge(10, 96, 2, None, None, None, None, 1, 0, None) == 2
+    assert L.dfa_lse_merge(10, 128, 0, None, None, None, None, 1, 0, None) == 1
+    assert L.dfa_lse_merge(10, 128, 2, None, None, None, None, 0, 1, None) == 1
+
+
+def test_chunk_map_validation(L):
+    desc = dfa.make_desc(1, 1, 1, 64, 64)
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) & ~255)
+    good = dfa.pos_map(1, (64, 0), (0, 0))
+    # lengths not adding up
+    pair = dfa.ChunkPair(dfa.pos_map(1, (32, 0), (0, 0)), good)
+    assert L.dfa_chunk_fwd(ctypes.byref(desc), ctypes.byref(pair), 64, 64, p, p, p, p, p, p,
+                           256, None) == 1
+    # non-monotone two-segment map
+    pair = dfa.ChunkPair(dfa.pos_map(2, (32, 32), (100, 0)), good)
+    assert L.dfa_chunk_fwd(ctypes.byref(desc), ctypes.byref(pair), 64, 64, p, p, p, p, p, p,
+                           256, None) == 2
+
+
+@pytest.mark.parametrize("kind,N,P,stripe", [("contiguous", 256, 4, 1), ("balanced", 256, 4, 1),
+                                             ("striped", 256, 4, 1), ("striped", 1024, 4, 64),
+                                             ("balanced", 4096, 16, 1), ("striped", 4096, 8, 1),
+                                             ("contiguous", 4096, 8, 1)])
+def test_partition_maps_match_oracle(orc, kind, N, P, stripe):
+    n = N // P
+    for p in range(P):
+        m = dfa.partition_map(N, P, p, kind, stripe)
+        pos = np.empty(n, dtype=np.int64)
+        start = 0
+        for t in range(m.nseg):
+            x = np.arange(m.len[t])
+            pos[start:start + m.len[t]] = m.base[t] + (x // m.blk) * m.blk_stride + x % m.blk
+            start += m.len[t]
+        assert np.array_equal(pos, orc.partition_pos(kind, N, P, p, stripe))
+
+
+@pytest.mark.parametrize("kind,N,P,stripe", [("contiguous", 256, 4, 1), ("balanced", 256, 4, 1),
+                                             ("striped", 256, 4, 1), ("balanced", 2048, 8, 1),
+                                             ("striped", 2048, 8, 1), ("contiguous", 2048, 8, 1),
+                                             ("striped", 2048, 4, 64)])
+@pytest.mark.parametrize("tiles", [(64, 64), (128, 128), (256, 128)])
+def test_schedule_bit_exact_against_oracle(orc, kind, N, P, stripe, tiles):
+    tm, tn = tiles
+    s = dfa.make_schedule(N, P, kind, stripe, tile_m=tm, tile_n=tn)
+    cnt = orc.pair_counts(kind, N, P, stripe)
+    for p in range(P):
+        for st in range(P):
+            w = (p - st) % P
+            assert s["pair_tokens"][p, st] == cnt[p, w]
+            cls = orc.tile_classes(kind, N, P, p, w, tm, tn, stripe)
+            got = s["tile_counts"][p, st]
+            assert got[0] == (cls == 0).sum()
+            assert got[1] == (cls == 1).sum()
+            assert got[2] == (cls == 2).sum()
+    assert s["total_pairs"] == N * (N + 1) // 2
+    nonempty = (cnt > 0).sum()
+    assert abs(s["eta_slots"] - nonempty / P**2) < 1e-15
+
+
+def test_schedule_eta_closed_forms():
+    # contiguous: (P+1)/(2P) non-empty slots; folded and striped keep every slot busy
+    for P in (2, 4, 8):
+        s = dfa.make_schedule(64 * P, P, "contiguous", tile_m=64, tile_n=64)
+        assert abs(s["eta_slots"] - (P + 1) / (2 * P)) < 1e-15
+        for kind in ("balanced", "striped"):
+            assert dfa.make_schedule(64 * P, P, kind)["eta_slots"] == 1.0
+    # striped lockstep utilisation: every step's max is n(n+1)/2 over total N(N+1)/2
+    N, P = 1024, 8
+    n = N // P
+    s = dfa.make_schedule(N, P, "striped")
+    assert abs(s["eta_flops"] - (N * (N + 1) / 2) / (P * P * n * (n + 1) / 2)) < 1e-12
