@@ -1,0 +1,404 @@
+"""Benchmark: causal attention forward + backward on one GB300 (per rank).
+
+One step = the whole hot path over one batch of synthetic input:
+  permute Q, K, V, dO to the partition's worker-major order
+  -> forward over every (worker, ring step) chunk pair in one launch
+     (online-softmax merge of the ring steps on chip)
+  -> backward (D preprocess, recomputation kernel, dQ conversion)
+  -> un-permute O, LSE, dQ, dK, dV to natural order.
+Workload: Llama-7B attention layer at N = 131072 (B=1, H=32, d=128, causal,
+bf16 N(0,1) inputs from seed 2 with 1% of query rows x8), P = 8 striped.
+Throughput counts causal FLOPs only: fwd 4 d pairs, bwd 10 d pairs,
+pairs = B H N (N+1) / 2.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica (weak scaling); rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "causal attn fwd+bwd TFLOPS (bf16, 1 GB300) and % of dense BF16 tensor peak"
+WORKLOAD = "llama7b_128k"
+PARTITION = "striped"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a per-rank value over the default process group (identity when
+    no group is initialised).  Used only for timing, never on the data path."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = sorted(float(r[1]) for r in rows)
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_traffic(kernel_file: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    with open(source, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if d.get("source_sha256_16") != h:
+        return None
+    return d.get("dram_bytes_per_launch_full_size")
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args):
+    from long_context_flashattention_gb300 import dfa
+    from long_context_flashattention_gb300.inputs import WORKLOADS, make_workload
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    P, kind = w.P, PARTITION
+    dfa.lib()
+
+    # inputs, resident in HBM before timing (larger than L2: 1 GiB per tensor)
+    q, k, v, do = make_workload(w)
+    host = [t.pin_memory() for t in (q, k, v, do)]
+    qg, kg, vg, dog = (t.to(dev) for t in host)
+    bufs = {
+        "perm": [torch.empty_like(t) for t in (qg, kg, vg, dog)],
+        "o": torch.empty_like(qg), "lse": torch.empty(w.B, w.Hq, w.N, device=dev),
+        "dq": torch.empty_like(qg), "dk": torch.empty_like(kg), "dv": torch.empty_like(vg),
+        "out": [torch.empty_like(qg), torch.empty(w.B, w.Hq, w.N, device=dev),
+                torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)],
+    }
+    desc = dfa.desc_for(qg, kg, P=P, partition=kind)
+    ws = dfa.new_workspace(desc, dfa.OP_BWD, dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = {n: torch.cuda.Event(enable_timing=True) for n in ("f0", "f1", "b0", "b1")}
+
+    def step(inputs, record=False):
+        pq, pk, pv, pdo = bufs["perm"]
+        for src, dst in zip(inputs, bufs["perm"]):
+            dfa.permute(src, P, kind, out=dst)
+        if record:
+            ev["f0"].record(stream)
+        dfa.attn_fwd(pq, pk, pv, P=P, partition=kind, ws=ws, out=bufs["o"], lse=bufs["lse"])
+        if record:
+            ev["f1"].record(stream)
+            ev["b0"].record(stream)
+        dfa.attn_bwd(pq, pk, pv, bufs["o"], pdo, bufs["lse"], P=P, partition=kind, ws=ws,
+                     dq=bufs["dq"], dk=bufs["dk"], dv=bufs["dv"])
+        if record:
+            ev["b1"].record(stream)
+        for src, dst in zip((bufs["o"], bufs["lse"], bufs["dq"], bufs["dk"], bufs["dv"]),
+                            bufs["out"]):
+            dfa.permute(src, P, kind, inverse=True, out=dst)
+
+    launches_per_step = 4 + 1 + 3 + 5
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step((qg, kg, vg, dog))
+    dfa.stream_status(ws)
+    barrier()
+
+    fwd_ms, bwd_ms = [], []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t0.record(stream)
+        for _ in range(args.steps):
+            step((qg, kg, vg, dog), record=True)
+            # per-call events; read after the region (no sync inside)
+            fwd_ms.append((ev["f0"], ev["f1"]))
+            bwd_ms.append((ev["b0"], ev["b1"]))
+            ev = {n: torch.cuda.Event(enable_timing=True) for n in ("f0", "f1", "b0", "b1")}
+        t1.record(stream)
+        barrier()
+    dfa.stream_status(ws)
+    step_ms = t0.elapsed_time(t1) / args.steps
+    fwd_call_ms = sum(a.elapsed_time(b) for a, b in fwd_ms) / len(fwd_ms)
+    bwd_call_ms = sum(a.elapsed_time(b) for a, b in bwd_ms) / len(bwd_ms)
+    step_ms = reduce_max(step_ms, dev)
+
+    # end to end through the public API: pinned host inputs -> device -> step -> host
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in bufs["out"]]
+    e2e_in = [torch.empty_like(t) for t in (qg, kg, vg, dog)]
+    e2e_steps = max(1, min(args.steps, 3))
+
+    def e2e_step():
+        for h, dsrc in zip(host, e2e_in):
+            dsrc.copy_(h, non_blocking=True)
+        step(e2e_in)
+        for h, dres in zip(h_out, bufs["out"]):
+            h.copy_(dres, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    # standalone LSE merge at this workload's size (k = P partials per row)
+    rows = w.B * w.Hq * w.N
+    del e2e_in
+    parts_o = torch.randn(P, rows, w.d, device=dev)
+    parts_l = 4 * torch.randn(P, rows, device=dev)
+    m_out = torch.empty(rows, w.d, dtype=torch.bfloat16, device=dev)
+    m_lse = torch.empty(rows, device=dev)
+    for _ in range(3):
+        dfa.lse_merge(parts_o, parts_l, out_fp32=False, o_out=m_out, lse_out=m_lse)
+    m0 = torch.cuda.Event(enable_timing=True)
+    m1 = torch.cuda.Event(enable_timing=True)
+    reps = 10
+    torch.cuda.synchronize(dev)
+    m0.record(stream)
+    for _ in range(reps):
+        dfa.lse_merge(parts_o, parts_l, out_fp32=False, o_out=m_out, lse_out=m_lse)
+    m1.record(stream)
+    torch.cuda.synchronize(dev)
+    merge_ms = m0.elapsed_time(m1) / reps
+    merge_bytes = rows * (P * (4 * w.d + 4) + (2 * w.d + 4))
+    del parts_o, parts_l
+
+    pk, src = peaks()
+    flops = w.flops_fwd + w.flops_bwd
+    value = flops * world / (step_ms * 1e-3) / 1e12
+    bwd_tflops = w.flops_bwd / (bwd_call_ms * 1e-3) / 1e12
+    fwd_tflops = w.flops_fwd / (fwd_call_ms * 1e-3) / 1e12
+    peak_s = pk["bf16_tflops_sustained"]
+    merge_gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
+    bwd_src = os.path.join(ROOT, "long_context_flashattention_gb300", "csrc", "dfa_bwd.cu")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, 1% of query rows x8)",
+        "config": {"workload": f"{w.name} causal, P={P} {kind} partition, fused ring steps",
+                   "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "P": P,
+                   "partition": kind, "per_rank_batch": w.B,
+                   "l2": "inputs larger than L2 (1 GiB per tensor), no flush"},
+        "pct_of_peak": round(100 * value / world / peak_s, 2),
+        "pct_of_peak_basis": f"bf16_tflops_sustained {peak_s} ({src})",
+        "fwd_tflops": round(fwd_tflops, 2),
+        "bwd_tflops": round(bwd_tflops, 2),
+        "fwd_ms": round(fwd_call_ms, 3),
+        "bwd_ms": round(bwd_call_ms, 3),
+        "roofline": {
+            "kernel": "dfa::bwd::attn_bwd_kernel (timed over the dfa_attn_bwd call: D "
+                      "preprocess + main kernel + dQ convert)",
+            "bound": "tensor", "achieved": round(bwd_tflops, 2), "peak": peak_s,
+            "unit": "TFLOP/s", "frac": round(bwd_tflops / peak_s, 4),
+            "peak_source": f"{src} bf16_tflops_sustained",
+            "traffic": kernel_traffic("attn_bwd_kernel_llama7b_128k.json", bwd_src),
+        },
+        "merge": {"kernel": "dfa::lse_merge_kernel", "k": P, "rows": rows,
+                  "bytes": merge_bytes, "ms": round(merge_ms, 4),
+                  "achieved": round(merge_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                  "frac": round(merge_gbs / pk["hbm_gbs"], 4)},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(q, k, v, do, w, budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle arm (baseline / reference)
+# ----------------------------------------------------------------------------
+def cpu_baseline(q, k, v, do, w, budget_s=15.0):
+    """The fp64 oracle, as it stands, on the host cores: forward and dQ of
+    seeded sampled query rows of the same workload, in batches until the time
+    budget is used.  FLOPs counted: 4 d (i+1) per forward row and 6 d (i+1)
+    per dQ row (scores, dP and dQ), i the row's position."""
+    import numpy as np
+
+    import oracle
+    from long_context_flashattention_gb300.inputs import sample_rows
+    cores = oracle.num_threads()
+    rows_all = np.array(sample_rows(w.B, w.Hq, w.N, 1 << 16, seed=w.seed + 2000))
+    rng = np.random.default_rng(w.seed)
+    rng.shuffle(rows_all)
+    done, flops, t_used, batch = 0, 0.0, 0.0, 64
+    while t_used < budget_s and done < len(rows_all):
+        r = rows_all[done:done + batch]
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, rows=r)
+        oracle.attn_bwd_q_rows(q, k, v, do, r)
+        t_used += time.perf_counter() - t0
+        i = (r % w.N) + 1
+        flops += float((4 * w.d * i).sum() + (6 * w.d * i).sum())
+        done += len(r)
+        batch = min(batch * 2, 512)
+    value = flops / t_used / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} seeded sampled query rows of {w.name}: fp64 forward row + dQ "
+                      f"row each ({t_used:.1f} s)",
+            "seconds": round(t_used, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from long_context_flashattention_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS[args.workload]
+    q, k, v, do = make_workload(w)
+    per = []
+    for _ in range(args.warmup):
+        cpu_baseline(q, k, v, do, w, budget_s=2.0)
+    t_total = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cb = cpu_baseline(q, k, v, do, w, budget_s=args.cpu_seconds / max(1, args.steps))
+        t_total += time.perf_counter() - t0
+        per.append(cb["value"])
+    value = sum(per) / len(per)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t_total / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} causal, P={w.P} {PARTITION} partition",
+                   "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"],
+                         "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dfa", choices=["dfa", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name from inputs.WORKLOADS (default: the 128K Llama-7B layer)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
