@@ -49,7 +49,8 @@ def check_o(o_gpu, o_ref, name="O"):
 def check_lse(l_gpu, l_ref):
     got = _np(l_gpu)
     both_inf = np.isneginf(got) & np.isneginf(l_ref)
-    err = np.where(both_inf, 0.0, np.abs(got - l_ref))
+    with np.errstate(invalid="ignore"):
+        err = np.where(both_inf, 0.0, np.abs(got - l_ref))
     assert err.max() <= LSE_TOL, f"LSE max err {err.max():.3e}"
 
 
@@ -59,7 +60,13 @@ def rel_fro(got, ref):
 
 
 def check_grad(g, ref, name):
-    r = rel_fro(_np(g), ref)
+    got = _np(g)
+    if np.linalg.norm(ref) == 0.0:
+        # an exactly-zero gradient (e.g. dQ of a row that sees one key): the
+        # pinned bound is absolute
+        assert np.abs(got).max() <= 1e-6, f"{name}: max |g| {np.abs(got).max():.3e} for zero ref"
+        return
+    r = rel_fro(got, ref)
     assert r <= G_TOL, f"{name}: relative Frobenius error {r:.3e}"
 
 
