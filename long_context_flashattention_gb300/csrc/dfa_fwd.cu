@@ -9,7 +9,8 @@
 // O / l and LSE = m * scale + ln l.  Fully masked tiles are never visited;
 // tiles entirely in the past need no mask.
 //
-// GB300 mapping (one persistent CTA per SM, 320 threads):
+// GB300 mapping (one persistent CTA per SM, 384 threads = 3 warpgroups;
+// warps 10-11 only give their registers to the math warpgroups):
 //   warp 9      TMA producer: Q tiles (2 x 128 rows) per unit, K/V tiles
 //               (128 rows) through a KS-stage ring, 128-byte swizzle.
 //   warp 8      MMA issuer (one thread): S_t = Q_t K^T into TMEM (fp32),
@@ -31,7 +32,12 @@ namespace dfa {
 
 namespace fwd {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;      // three warpgroups
+// Launch: 384 threads x 168 registers = 64512.  The producer/MMA warpgroup
+// drops to 40, the two math warpgroups rise to 232: 128 * (232 + 232 + 40)
+// = 64512, the launch's total.
+constexpr int kRegsMath = 192;
+constexpr int kRegsCtl = 120;
 constexpr int kRowsPerUnit = 256;  // two 128-row query tiles
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -125,154 +131,158 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 9) {
-        // ------------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tmap(&tmq);
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
-            uint32_t kc = 0, qc = 0;
-            for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-                Unit un = decode_unit(p.units, p.BH, kRowsPerUnit, u, false);
-                if (unit_tiles(p, un) == 0)
-                    continue;
-                const int b = un.slice / p.Hq, h = un.slice % p.Hq;
-                const int zk = b * p.Hkv + h / p.G;
-                if (qc > 0 && !mbar_wait(&bar[C::QEMPTY], (qc - 1) & 1, wctx, 10))
-                    goto producer_done;
-                mbar_arrive_expect_tx(&bar[C::QFULL], 2 * C::kTile);
-                {
-                    const int qrow = un.chunk * p.chunk_q + un.row0;
+    if (warp >= 8) {
+        reg_dealloc<kRegsCtl>();
+        if (warp == 9) {
+            // ------------------------------------------------------------- producer
+            if (lane == 0) {
+                prefetch_tmap(&tmq);
+                prefetch_tmap(&tmk);
+                prefetch_tmap(&tmv);
+                uint32_t kc = 0, qc = 0;
+                for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+                    Unit un = decode_unit(p.units, p.BH, kRowsPerUnit, u, false);
+                    if (unit_tiles(p, un) == 0)
+                        continue;
+                    const int b = un.slice / p.Hq, h = un.slice % p.Hq;
+                    const int zk = b * p.Hkv + h / p.G;
+                    if (qc > 0 && !mbar_wait(&bar[C::QEMPTY], (qc - 1) & 1, wctx, 10))
+                        goto producer_done;
+                    mbar_arrive_expect_tx(&bar[C::QFULL], 2 * C::kTile);
+                    {
+                        const int qrow = un.chunk * p.chunk_q + un.row0;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
+                        for (int t = 0; t < 2; ++t)
 #pragma unroll
-                        for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_3d(smem + C::kQ0 + t * C::kTile + hb * 16384, &tmq,
-                                        &bar[C::QFULL], hb * 64, qrow + t * 128, un.slice);
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_3d(smem + C::kQ0 + t * C::kTile + hb * 16384, &tmq,
+                                            &bar[C::QFULL], hb * 64, qrow + t * 128, un.slice);
+                    }
+                    ++qc;
+                    for (int s = 0; s < p.nkv; ++s) {
+                        StepTiles st = step_tiles(p, un, s);
+                        for (int j = 0; j < st.jv; ++j) {
+                            const int ks = kc % C::kStages;
+                            const uint32_t n = kc / C::kStages;
+                            const int krow = st.c * p.chunk_k + j * 128;
+                            if (kc >= (uint32_t)C::kStages &&
+                                !mbar_wait(&bar[C::KEMPTY + ks], (n - 1) & 1, wctx, 11))
+                                goto producer_done;
+                            mbar_arrive_expect_tx(&bar[C::KFULL + ks], C::kTile);
+#pragma unroll
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_3d(smem + C::kK0 + ks * C::kTile + hb * 16384, &tmk,
+                                            &bar[C::KFULL + ks], hb * 64, krow, zk);
+                            if (kc >= (uint32_t)C::kStages &&
+                                !mbar_wait(&bar[C::VEMPTY + ks], (n - 1) & 1, wctx, 12))
+                                goto producer_done;
+                            mbar_arrive_expect_tx(&bar[C::VFULL + ks], C::kTile);
+#pragma unroll
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_3d(smem + C::kV0 + ks * C::kTile + hb * 16384, &tmv,
+                                            &bar[C::VFULL + ks], hb * 64, krow, zk);
+                            ++kc;
+                        }
+                    }
                 }
-                ++qc;
-                for (int s = 0; s < p.nkv; ++s) {
-                    StepTiles st = step_tiles(p, un, s);
-                    for (int j = 0; j < st.jv; ++j) {
-                        const int ks = kc % C::kStages;
-                        const uint32_t n = kc / C::kStages;
-                        const int krow = st.c * p.chunk_k + j * 128;
-                        if (kc >= (uint32_t)C::kStages &&
-                            !mbar_wait(&bar[C::KEMPTY + ks], (n - 1) & 1, wctx, 11))
-                            goto producer_done;
-                        mbar_arrive_expect_tx(&bar[C::KFULL + ks], C::kTile);
-#pragma unroll
-                        for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_3d(smem + C::kK0 + ks * C::kTile + hb * 16384, &tmk,
-                                        &bar[C::KFULL + ks], hb * 64, krow, zk);
-                        if (kc >= (uint32_t)C::kStages &&
-                            !mbar_wait(&bar[C::VEMPTY + ks], (n - 1) & 1, wctx, 12))
-                            goto producer_done;
-                        mbar_arrive_expect_tx(&bar[C::VFULL + ks], C::kTile);
-#pragma unroll
-                        for (int hb = 0; hb < D / 64; ++hb)
-                            tma_load_3d(smem + C::kV0 + ks * C::kTile + hb * 16384, &tmv,
-                                        &bar[C::VFULL + ks], hb * 64, krow, zk);
-                        ++kc;
+            producer_done:
+                // Drain: on an abort, give copies already issued a bounded chance
+                // to land before the CTA's shared memory is released.
+                if (*abort_flag) {
+                    uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 2000000ull) {
                     }
                 }
             }
-        producer_done:
-            // Drain: on an abort, give copies already issued a bounded chance
-            // to land before the CTA's shared memory is released.
-            if (*abort_flag) {
-                uint64_t t0 = globaltimer_ns();
-                while (globaltimer_ns() - t0 < 2000000ull) {
-                }
-            }
-        }
-    } else if (warp == 8) {
-        // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-            const uint32_t sQ = smem_u32(smem + C::kQ0);
-            const uint32_t sK = smem_u32(smem + C::kK0);
-            const uint32_t sV = smem_u32(smem + C::kV0);
-            const uint32_t tS0 = tmem, tS1 = tmem + 128;
-            const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
-            uint32_t kc = 0, qc = 0, pc0 = 0, pc1 = 0;
+        } else if (warp == 8) {
+            // ------------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+                constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+                const uint32_t sQ = smem_u32(smem + C::kQ0);
+                const uint32_t sK = smem_u32(smem + C::kK0);
+                const uint32_t sV = smem_u32(smem + C::kV0);
+                const uint32_t tS0 = tmem, tS1 = tmem + 128;
+                const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+                uint32_t kc = 0, qc = 0, pc0 = 0, pc1 = 0;
 
-            auto issue_s = [&](uint32_t tS, uint32_t qoff, int ks) {
+                auto issue_s = [&](uint32_t tS, uint32_t qoff, int ks) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_ss(tS, sdesc_sw128(sQ + qoff + off, 16, 1024),
-                           sdesc_sw128(sK + ks * C::kTile + off, 16, 1024), idS, kk > 0);
-                }
-            };
-            auto issue_pv = [&](uint32_t tO, uint32_t tP, int vs, bool acc) {
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tS, sdesc_sw128(sQ + qoff + off, 16, 1024),
+                               sdesc_sw128(sK + ks * C::kTile + off, 16, 1024), idS, kk > 0);
+                    }
+                };
+                auto issue_pv = [&](uint32_t tO, uint32_t tP, int vs, bool acc) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tO, tP + kk * 8,
-                           sdesc_sw128(sV + vs * C::kTile + kk * 2048, 16384, 1024), idO,
-                           (acc || kk > 0) ? 1u : 0u);
-            };
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tO, tP + kk * 8,
+                               sdesc_sw128(sV + vs * C::kTile + kk * 2048, 16384, 1024), idO,
+                               (acc || kk > 0) ? 1u : 0u);
+                };
 
-            for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-                Unit un = decode_unit(p.units, p.BH, kRowsPerUnit, u, false);
-                const int total = unit_tiles(p, un);
-                if (total == 0)
-                    continue;
-                if (!mbar_wait(&bar[C::QFULL], qc & 1, wctx, 20))
-                    goto mma_done;
-                ++qc;
-                tc_fence_after();
-                {
-                    const int ks = kc % C::kStages;
-                    if (!mbar_wait(&bar[C::KFULL + ks], (kc / C::kStages) & 1, wctx, 21))
+                for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+                    Unit un = decode_unit(p.units, p.BH, kRowsPerUnit, u, false);
+                    const int total = unit_tiles(p, un);
+                    if (total == 0)
+                        continue;
+                    if (!mbar_wait(&bar[C::QFULL], qc & 1, wctx, 20))
                         goto mma_done;
+                    ++qc;
                     tc_fence_after();
-                    issue_s(tS0, 0, ks);
-                    tc_commit(&bar[C::SFULL + 0]);
-                    issue_s(tS1, C::kTile, ks);
-                    tc_commit(&bar[C::SFULL + 1]);
-                    tc_commit(&bar[C::KEMPTY + ks]);
-                }
-                for (int it = 0; it < total; ++it) {
-                    const int vs = kc % C::kStages;
-                    const bool has_next = it + 1 < total;
-                    const int ks2 = (kc + 1) % C::kStages;
-                    if (!mbar_wait(&bar[C::VFULL + vs], (kc / C::kStages) & 1, wctx, 22))
-                        goto mma_done;
-                    if (!mbar_wait(&bar[C::PFULL + 0], pc0 & 1, wctx, 23))
-                        goto mma_done;
-                    ++pc0;
-                    tc_fence_after();
-                    issue_pv(tO0, tS0, vs, it > 0);
-                    if (has_next) {
-                        if (!mbar_wait(&bar[C::KFULL + ks2], ((kc + 1) / C::kStages) & 1, wctx,
-                                       24))
+                    {
+                        const int ks = kc % C::kStages;
+                        if (!mbar_wait(&bar[C::KFULL + ks], (kc / C::kStages) & 1, wctx, 21))
                             goto mma_done;
                         tc_fence_after();
-                        issue_s(tS0, 0, ks2);
+                        issue_s(tS0, 0, ks);
                         tc_commit(&bar[C::SFULL + 0]);
-                    }
-                    if (!mbar_wait(&bar[C::PFULL + 1], pc1 & 1, wctx, 25))
-                        goto mma_done;
-                    ++pc1;
-                    tc_fence_after();
-                    issue_pv(tO1, tS1, vs, it > 0);
-                    tc_commit(&bar[C::VEMPTY + vs]);
-                    if (has_next) {
-                        issue_s(tS1, C::kTile, ks2);
+                        issue_s(tS1, C::kTile, ks);
                         tc_commit(&bar[C::SFULL + 1]);
-                        tc_commit(&bar[C::KEMPTY + ks2]);
+                        tc_commit(&bar[C::KEMPTY + ks]);
                     }
-                    ++kc;
+                    for (int it = 0; it < total; ++it) {
+                        const int vs = kc % C::kStages;
+                        const bool has_next = it + 1 < total;
+                        const int ks2 = (kc + 1) % C::kStages;
+                        if (!mbar_wait(&bar[C::VFULL + vs], (kc / C::kStages) & 1, wctx, 22))
+                            goto mma_done;
+                        if (!mbar_wait(&bar[C::PFULL + 0], pc0 & 1, wctx, 23))
+                            goto mma_done;
+                        ++pc0;
+                        tc_fence_after();
+                        issue_pv(tO0, tS0, vs, it > 0);
+                        if (has_next) {
+                            if (!mbar_wait(&bar[C::KFULL + ks2], ((kc + 1) / C::kStages) & 1, wctx,
+                                           24))
+                                goto mma_done;
+                            tc_fence_after();
+                            issue_s(tS0, 0, ks2);
+                            tc_commit(&bar[C::SFULL + 0]);
+                        }
+                        if (!mbar_wait(&bar[C::PFULL + 1], pc1 & 1, wctx, 25))
+                            goto mma_done;
+                        ++pc1;
+                        tc_fence_after();
+                        issue_pv(tO1, tS1, vs, it > 0);
+                        tc_commit(&bar[C::VEMPTY + vs]);
+                        if (has_next) {
+                            issue_s(tS1, C::kTile, ks2);
+                            tc_commit(&bar[C::SFULL + 1]);
+                            tc_commit(&bar[C::KEMPTY + ks2]);
+                        }
+                        ++kc;
+                    }
+                    tc_commit(&bar[C::OFULL + 0]);
+                    tc_commit(&bar[C::OFULL + 1]);
+                    tc_commit(&bar[C::QEMPTY]);
                 }
-                tc_commit(&bar[C::OFULL + 0]);
-                tc_commit(&bar[C::OFULL + 1]);
-                tc_commit(&bar[C::QEMPTY]);
+            mma_done:;
             }
-        mma_done:;
         }
     } else {
+        reg_alloc<kRegsMath>();
         // ------------------------------------------------------------- softmax
         const int t = warp >> 2;            // query tile of this warpgroup
         const int wq = warp & 3;            // TMEM lane quarter

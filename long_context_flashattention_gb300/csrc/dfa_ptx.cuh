@@ -98,7 +98,7 @@ struct WaitCtx {
 // Wait until the barrier's phase with the given parity has completed.
 // Returns false (and leaves the caller to unwind) when the CTA is aborting or
 // the limit passed; the first to time out records `where` in the status word.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+static __device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtx& w,
                                             int where)
 {
     uint64_t t0 = globaltimer_ns();
@@ -330,6 +330,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r)
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Register rebalancing between warpgroups (all four warps of a warpgroup
+// execute the same instruction).  A kernel launched with T threads at R
+// registers each may redistribute at most T * R registers in total.
+// ---------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void reg_dealloc()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_alloc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------------------
