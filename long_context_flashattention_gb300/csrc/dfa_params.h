@@ -66,12 +66,14 @@ DFA_HD int32_t map_count_le(const DevMap& m, int32_t x)
 
 DFA_HD int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
-// Work units.  The query rows of every chunk are cut into segments (runs of
-// rows inside one map segment) and each segment into units of `rows_per_unit`
-// rows; units are replicated over the BH (batch x head) slices.  Units are
-// issued longest-first: by segment in the order given (host sorts segments
-// by descending position), or, with tile_major, round by round across
-// equal-length segments.
+// Work units.  The rows of every chunk are cut into segments (runs of rows
+// inside one map segment) and each segment into units of `rows_per_unit`
+// rows; units are replicated over the BH (batch x head) slices.  Inside a
+// slice, units are issued longest-first: by segment in the order given (the
+// host sorts segments by position), or, with tile_major, round by round across
+// equal-length segments.  Slices are issued one after another (all units of
+// slice 0, then slice 1, ...), so that the CTAs running at the same time share
+// one head's K/V (forward) or Q/dO/dQ rows (backward) in L2.
 struct UnitTable {
     int32_t nsegs;
     int32_t tile_major;
@@ -94,8 +96,9 @@ DFA_HD Unit decode_unit(const UnitTable& t, int32_t nslices, int32_t rows_per_un
                         bool reverse)
 {
     Unit r;
-    int32_t rank = u / nslices;
-    r.slice = u % nslices;
+    (void)nslices;
+    int32_t rank = u % t.units_per_slice;
+    r.slice = u / t.units_per_slice;
     int32_t seg, k;
     if (t.tile_major) {
         seg = rank % t.nsegs;
