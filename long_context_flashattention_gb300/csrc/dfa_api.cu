@@ -371,7 +371,7 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.timeout_ns = kDefaultTimeoutNs;
     if (p.total_units == 0)
         return DFA_OK;
-    const int bq = d.d == 128 ? 64 : 128;  // query rows per backward step
+    const int bq = bwd_query_rows_per_step();
     CUtensorMap tq, tk, tv, tdo;
     dfa_status s;
     const int64_t BHq = (int64_t)d.B * d.Hq, BHkv = (int64_t)d.B * d.Hkv;

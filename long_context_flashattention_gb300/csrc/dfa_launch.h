@@ -21,6 +21,7 @@ cudaError_t launch_attn_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
                             int grid, cudaStream_t stream);
 int bwd_rows_per_unit();
+int bwd_query_rows_per_step();
 
 cudaError_t launch_lse_merge(int64_t rows, int d, int k, const float* o_parts,
                              const float* lse_parts, void* o_out, float* lse_out, int out_fp32,
