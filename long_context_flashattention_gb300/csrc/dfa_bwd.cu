@@ -10,26 +10,28 @@
 // Masking and tile skipping follow the forward (Striped Attention Guide,
 // "Intra-Block vs. Inter-Block Masking Logic").
 //
-// GB300 mapping: one persistent CTA per SM, 384 threads = 3 warpgroups.  A
+// GB300 mapping: one persistent CTA per SM, 512 threads = 4 warpgroups.  A
 // work unit is one 128-row key/value tile; it meets every visible 64-row query
 // tile ("step") of every query head of its group.  Key rows sit on TMEM lanes,
 // so dK and dV accumulate in TMEM for the whole unit.
-//   warp 9      producer: K, V once per unit (TMA); per step the Q and dO
+//   warp 13     producer: K, V once per unit (TMA); per step the Q and dO
 //               tiles (TMA) and the LSE / D values into a 3-stage ring.
-//   warp 8      MMA issuer.  Per step n, with TMEM buffer b = n & 1:
+//   warp 12     MMA issuer.  Per step n, with TMEM buffer b = n & 1:
 //                 S^T = K Q^T and dP^T = V dO^T of step n+1 are issued
 //                 BEFORE the step-n products, so the tensor core computes
 //                 them while the softmax warps work on step n;
 //                 dV += P^T dO, dK += dS^T Q (A operand read from TMEM);
 //                 dQ^T = K^T dS^T into the S^T columns of buffer b (their P^T
 //                 has been consumed by dV).
-//   warps 0-3   one thread per key row: P^T = exp2(S^T c - LSE log2 e),
-//               dS^T = P^T (dP^T - D), written as bf16 over S^T / dP^T and
-//               dS^T also into a double-buffered swizzled SMEM tile; at the
-//               end of a unit they scale and store dK, dV.
-//   warps 4-7   drain each step's dQ^T tile from TMEM into the fp32 dQ
+//   warps 0-7   two warpgroups, one thread per key row, each on 32 of the
+//               step's 64 query columns: P^T = exp2(S^T c - LSE log2 e),
+//               dS^T = P^T (dP^T - D) (packed f32x2 arithmetic), written as
+//               bf16 over S^T / dP^T and dS^T also into a double-buffered
+//               swizzled SMEM tile; at the end of a unit the first warpgroup
+//               stores dK (scaled), the second dV.
+//   warps 8-11  drain each step's dQ^T tile from TMEM into the fp32 dQ
 //               accumulator with coalesced atomics.
-//   warps 10-11 give their registers to the math warpgroups.
+//   warps 14-15 give their registers to the other warpgroups.
 // TMEM columns: dK [0,d) dV [d,2d), then per buffer b: S^T [2d+128b, +64),
 // dP^T [2d+128b+64, +64).  d = 64 uses the same path: the K tile is padded
 // to 128 columns with zeros so that dQ^T has 128 lanes.
@@ -45,12 +47,14 @@ namespace dfa {
 
 namespace bwd {
 
-constexpr int kThreads = 384;
-// Launch: 384 threads x 168 registers = 64512.  The producer/MMA warpgroup
-// drops to 120, the two math warpgroups rise to 192: 128 * (192 + 192 + 120)
-// = 64512, the launch's total.
-constexpr int kRegsMath = 192;
+constexpr int kThreads = 512;
+// Launch: 512 threads x 128 registers = 65536.  Rebalanced per warpgroup:
+// 128 * (kRegsSoft * 2 + kRegsDrain + kRegsCtl) = 65536.
+constexpr int kRegsSoft = 152;
+constexpr int kRegsDrain = 88;
 constexpr int kRegsCtl = 120;
+static_assert(2 * kRegsSoft + kRegsDrain + kRegsCtl == 512, "register budget");
+constexpr int kWarpMma = 12, kWarpProducer = 13;
 constexpr int kKvRows = 128;
 constexpr int BQ = 64;  // query rows per step
 
@@ -180,21 +184,22 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
                     __syncwarp();
                     if (*sh.abort_flag)
                         return;
-                    // LSE in log2 units (-inf -> +inf, so that P = 0) and D
+                    // -LSE in log2 units (a row without keys gives -inf, so that
+                    // P = 0; so do rows past the chunk) and -D
                     const int32_t m0 = i * BQ;
                     const size_t rbase = (size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q + m0;
                     float* sl = (float*)(smem + C::kLse0 + st * BQ * 4);
                     float* sd = (float*)(smem + C::kDel0 + st * BQ * 4);
 #pragma unroll
                     for (int c = lane; c < BQ; c += 32) {
-                        float l2 = INFINITY, dl = 0.f;
+                        float nl = -INFINITY, nd = 0.f;
                         if (m0 + c < p.chunk_q) {
                             const float lv = p.lse[rbase + c];
-                            l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
-                            dl = p.delta[rbase + c];
+                            nl = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
+                            nd = -p.delta[rbase + c];
                         }
-                        sl[c] = l2;
-                        sd[c] = dl;
+                        sl[c] = nl;
+                        sd[c] = nd;
                     }
                     __syncwarp();
                     if (lane == 0) {
@@ -305,7 +310,9 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
 }
 
 // ---------------------------------------------------------------------------
-// P^T / dS^T warpgroup (warps 0-3), one thread per key row; dK/dV epilogue
+// P^T / dS^T warpgroups (warps 0-7), one thread per key row, warpgroup h on
+// query columns [32 h, 32 h + 32) of each step; dK (h = 0) / dV (h = 1)
+// epilogue at the end of a unit.
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& sh,
@@ -314,9 +321,10 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     using C = Cfg<D>;
     uint64_t* bar = sh.bar;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = warp * 32 + lane;  // key row inside the unit tile (TMEM lane)
-    const uint32_t tl = sh.tmem + ((uint32_t)(warp * 32) << 16);
-    const float c2 = p.scale_log2;
+    const int h = warp >> 2;                 // column half of this warpgroup
+    const int r = (warp & 3) * 32 + lane;    // key row inside the unit tile (TMEM lane)
+    const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
@@ -339,57 +347,55 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                             return;
                         if (!mbar_wait(&bar[C::SFULL + b], (n >> 1) & 1, w, 71))
                             return;
+                        tc_fence_after();
+                        uint32_t sr[32], dr[32];
+                        tmem_ld32(tl + C::cS(b) + 32 * h, sr);
+                        tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
+                        const float* sl = (const float*)(sh.smem + C::kLse0 + st * BQ * 4) + 32 * h;
+                        const float* sd = (const float*)(sh.smem + C::kDel0 + st * BQ * 4) + 32 * h;
+                        const bool full = (i >= qr.ifull) && ((i + 1) * BQ <= p.chunk_q) &&
+                                          un.nvalid == kKvRows;
+                        const int qbase = i * BQ + 32 * h;
+                        tmem_ld_wait();
+                        tmem_reg_fence32(sr);
+                        tmem_reg_fence32(dr);
+                        uint32_t pp[16], dd[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            // two query columns 2j, 2j+1 at a time (f32x2)
+                            const uint64_t nl = *(const uint64_t*)(sl + 2 * j);
+                            const uint64_t nd = *(const uint64_t*)(sd + 2 * j);
+                            float a0, a1;
+                            f2unpack(f2fma(f2pack(__uint_as_float(sr[2 * j]),
+                                                  __uint_as_float(sr[2 * j + 1])),
+                                           c2x2, nl),
+                                     a0, a1);
+                            float p0 = ex2(a0), p1 = ex2(a1);
+                            if (!full) {
+                                const int q = qbase + 2 * j;
+                                p0 = (q >= qv && q < p.chunk_q) ? p0 : 0.f;
+                                p1 = (q + 1 >= qv && q + 1 < p.chunk_q) ? p1 : 0.f;
+                            }
+                            pp[j] = pack_bf16x2(p0, p1);
+                            float d0, d1;
+                            f2unpack(f2mul(f2pack(p0, p1),
+                                           f2add(f2pack(__uint_as_float(dr[2 * j]),
+                                                        __uint_as_float(dr[2 * j + 1])),
+                                                 nd)),
+                                     d0, d1);
+                            dd[j] = pack_bf16x2(d0, d1);
+                        }
+                        tmem_st16(tl + C::cS(b) + 16 * h, pp);
+                        tmem_st16(tl + C::cDP(b) + 16 * h, dd);
                         // the dQ MMA of step n - 2 has read dS^T buffer b
                         if (n >= 2 && !mbar_wait(&bar[C::DSEMPTY + b], ((n >> 1) - 1) & 1, w, 72))
                             return;
-                        tc_fence_after();
-                        const float* sl = (const float*)(sh.smem + C::kLse0 + st * BQ * 4);
-                        const float* sd = (const float*)(sh.smem + C::kDel0 + st * BQ * 4);
-                        const bool full = (i >= qr.ifull) && ((i + 1) * BQ <= p.chunk_q) &&
-                                          un.nvalid == kKvRows;
                         uint8_t* dsb = sh.smem + C::kDs0 + b * C::kDsBytes;
-                        // 32 query columns at a time
-#pragma unroll 1
-                        for (int c0 = 0; c0 < BQ; c0 += 32) {
-                            uint32_t sr[32], dr[32];
-                            tmem_ld32(tl + C::cS(b) + c0, sr);
-                            tmem_ld32(tl + C::cDP(b) + c0, dr);
-                            tmem_ld_wait();
-                            tmem_reg_fence32(sr);
-                            tmem_reg_fence32(dr);
-                            uint32_t pp[16], dd[16];
 #pragma unroll
-                            for (int c4 = 0; c4 < 8; ++c4) {
-                                const float4 l4 = *(const float4*)(sl + c0 + 4 * c4);
-                                const float4 d4 = *(const float4*)(sd + c0 + 4 * c4);
-                                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                                const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                                float pv[4], ds[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int c = 4 * c4 + e;
-                                    float pe = ex2(fmaf(__uint_as_float(sr[c]), c2, -lv[e]));
-                                    if (!full) {
-                                        const int q = i * BQ + c0 + c;
-                                        pe = (q >= qv && q < p.chunk_q) ? pe : 0.f;
-                                    }
-                                    pv[e] = pe;
-                                    ds[e] = pe * (__uint_as_float(dr[c]) - dv[e]);
-                                }
-                                pp[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-                                pp[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-                                dd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-                                dd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-                            }
-                            tmem_st16(tl + C::cS(b) + c0 / 2, pp);
-                            tmem_st16(tl + C::cDP(b) + c0 / 2, dd);
-                            // 32 bf16 = four 16-byte chunks of row r
-#pragma unroll
-                            for (int ch = 0; ch < 4; ++ch)
-                                *(uint4*)(dsb + sw128_offset(r, c0 / 8 + ch)) =
-                                    make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
-                                               dd[4 * ch + 3]);
-                        }
+                        for (int ch = 0; ch < 4; ++ch)
+                            *(uint4*)(dsb + sw128_offset(r, 4 * h + ch)) =
+                                make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
+                                           dd[4 * ch + 3]);
                         tmem_st_wait();
                         fence_proxy_async_smem();
                         tc_fence_before();
@@ -403,52 +409,49 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
             ++uc;
             tc_fence_after();
         }
-        // epilogue: dK (scaled) and dV rows of the unit
+        // epilogue: warpgroup 0 stores dK (scaled), warpgroup 1 dV
         const size_t orow = (size_t)un.slice * p.Lk + (size_t)un.chunk * p.chunk_k + un.row0 + r;
+        const uint32_t col = h == 0 ? C::cDK : C::cDV;
+        const float mul = h == 0 ? p.scale : 1.f;
+        void* outp = h == 0 ? p.dk : p.dv;
 #pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-            const uint32_t col = which == 0 ? C::cDK : C::cDV;
-            const float mul = which == 0 ? p.scale : 1.f;
-            void* outp = which == 0 ? p.dk : p.dv;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[32];
-                if (T > 0) {
-                    tmem_ld32(tl + col + c0, o);
-                    tmem_ld_wait();
-                    tmem_reg_fence32(o);
-                } else {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            if (T > 0) {
+                tmem_ld32(tl + col + c0, o);
+                tmem_ld_wait();
+                tmem_reg_fence32(o);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        o[e] = 0u;
-                }
-                if (!kvalid)
-                    continue;
-                if (p.dkv_mode == 0) {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        reinterpret_cast<__nv_bfloat16*>(outp) + orow * D + c0);
+                for (int e = 0; e < 32; ++e)
+                    o[e] = 0u;
+            }
+            if (!kvalid)
+                continue;
+            if (p.dkv_mode == 0) {
+                uint4* dst =
+                    reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(outp) + orow * D + c0);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul,
-                                                        __uint_as_float(o[8 * e + 1]) * mul),
-                                            pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul,
-                                                        __uint_as_float(o[8 * e + 3]) * mul),
-                                            pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul,
-                                                        __uint_as_float(o[8 * e + 5]) * mul),
-                                            pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul,
-                                                        __uint_as_float(o[8 * e + 7]) * mul));
-                } else {
-                    float4* dst =
-                        reinterpret_cast<float4*>(reinterpret_cast<float*>(outp) + orow * D + c0);
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * e + 0]) * mul,
+                                                    __uint_as_float(o[8 * e + 1]) * mul),
+                                        pack_bf16x2(__uint_as_float(o[8 * e + 2]) * mul,
+                                                    __uint_as_float(o[8 * e + 3]) * mul),
+                                        pack_bf16x2(__uint_as_float(o[8 * e + 4]) * mul,
+                                                    __uint_as_float(o[8 * e + 5]) * mul),
+                                        pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul,
+                                                    __uint_as_float(o[8 * e + 7]) * mul));
+            } else {
+                float4* dst =
+                    reinterpret_cast<float4*>(reinterpret_cast<float*>(outp) + orow * D + c0);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float4 a = dst[e];
-                        a.x += __uint_as_float(o[4 * e + 0]) * mul;
-                        a.y += __uint_as_float(o[4 * e + 1]) * mul;
-                        a.z += __uint_as_float(o[4 * e + 2]) * mul;
-                        a.w += __uint_as_float(o[4 * e + 3]) * mul;
-                        dst[e] = a;
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    float4 v = dst[e];
+                    v.x += __uint_as_float(o[4 * e + 0]) * mul;
+                    v.y += __uint_as_float(o[4 * e + 1]) * mul;
+                    v.z += __uint_as_float(o[4 * e + 2]) * mul;
+                    v.w += __uint_as_float(o[4 * e + 3]) * mul;
+                    dst[e] = v;
                 }
             }
         }
@@ -540,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar[C::SFULL + b], 1);
-            mbar_init(&bar[C::PFULL + b], 128);
-            mbar_init(&bar[C::DSFULL + b], 128);
+            mbar_init(&bar[C::PFULL + b], 256);
+            mbar_init(&bar[C::DSFULL + b], 256);
             mbar_init(&bar[C::DSEMPTY + b], 1);
             mbar_init(&bar[C::DQFULL + b], 1);
             mbar_init(&bar[C::DQEMPTY + b], 128);
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pad[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
-    if (warp == 8) {
+    if (warp == kWarpMma) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -565,9 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const Shared sh{smem, bar, abort_flag, *tmem_slot};
 
-    if (warp >= 8) {
+    if (warp >= 12) {
         reg_dealloc<kRegsCtl>();
-        if (warp == 9) {
+        if (warp == kWarpProducer) {
             producer<D>(p, sh, wctx, &tmq, &tmk, &tmv, &tmdo);
             if (lane == 0 && *abort_flag) {
                 // give copies already issued a bounded chance to land
@@ -575,21 +578,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (globaltimer_ns() - t0 < 2000000ull) {
                 }
             }
-        } else if (warp == 8 && lane == 0) {
+        } else if (warp == kWarpMma && lane == 0) {
             mma_issuer<D>(p, sh, wctx);
         }
-    } else if (warp < 4) {
-        reg_alloc<kRegsMath>();
-        softmax_grad<D>(p, sh, wctx);
-    } else {
-        reg_alloc<kRegsMath>();
+    } else if (warp >= 8) {
+        reg_dealloc<kRegsDrain>();
         dq_drain<D>(p, sh, wctx);
+    } else {
+        reg_alloc<kRegsSoft>();
+        softmax_grad<D>(p, sh, wctx);
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(sh.tmem, 512);
     }
