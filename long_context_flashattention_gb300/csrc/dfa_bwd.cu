@@ -121,6 +121,10 @@ __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& u
     return t * pr.G;
 }
 
+// TMEM column of the packed bf16 P^T / dS^T for K step kk (16 query rows):
+// query columns [32 h, 32 h + 32) are packed at columns [32 h, 32 h + 16).
+__host__ __device__ constexpr uint32_t ptcol(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+
 struct Shared {
     uint8_t* smem;
     uint64_t* bar;
@@ -282,7 +286,7 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ts(tmem + C::cDV, tmem + C::cS(b) + kk * 8,
+                mma_ts(tmem + C::cDV, tmem + C::cS(b) + ptcol(kk),
                        sdesc_sw128(sDO + st * C::kQTile + kk * 2048, BQ * 128, 1024), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             // dK += dS^T Q
@@ -291,7 +295,7 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ts(tmem + C::cDK, tmem + C::cDP(b) + kk * 8,
+                mma_ts(tmem + C::cDK, tmem + C::cDP(b) + ptcol(kk),
                        sdesc_sw128(sQ + st * C::kQTile + kk * 2048, BQ * 128, 1024), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&bar[C::QEMPTY + st]);
@@ -385,8 +389,10 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                      d0, d1);
                             dd[j] = pack_bf16x2(d0, d1);
                         }
-                        tmem_st16(tl + C::cS(b) + 16 * h, pp);
-                        tmem_st16(tl + C::cDP(b) + 16 * h, dd);
+                        // packed into the first 16 of this warpgroup's own 32 columns:
+                        // the other warpgroup may still be reading its half
+                        tmem_st16(tl + C::cS(b) + 32 * h, pp);
+                        tmem_st16(tl + C::cDP(b) + 32 * h, dd);
                         // the dQ MMA of step n - 2 has read dS^T buffer b
                         if (n >= 2 && !mbar_wait(&bar[C::DSEMPTY + b], ((n >> 1) - 1) & 1, w, 72))
                             return;
