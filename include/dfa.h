@@ -235,6 +235,31 @@ dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t 
 /* The position map of worker p under desc's partition (host only). */
 dfa_status dfa_partition_map(const dfa_attn_desc* desc, int32_t p, dfa_pos_map* out);
 
+/*
+ * dfa_attn_bwd_noalloc -- dfa_attn_bwd for callers that cannot allocate device
+ * memory.  The pages describe no counterpart: this is a library convenience.
+ *
+ * Who needs it: code that has tensor pointers but no allocator it may use --
+ * a plugin handed buffers by a host framework, a host callback, a loop that
+ * forbids cudaMalloc after start-up.  dfa_attn_bwd needs a workspace of
+ * 256 + B*Hq*N*(4d + 4) bytes (the fp32 dQ accumulator and D); here that
+ * scratch is a fixed 64 MiB array in device memory owned by the library, held
+ * by every GPU that loads the library until the process exits.  Problems
+ * whose scratch would exceed 64 MiB are rejected with DFA_ERR_WORKSPACE.
+ *
+ * Same arguments, layouts and results as dfa_attn_bwd, minus the workspace.
+ * This call allocates nothing.  Its first call on a device looks up the
+ * array's device address (with that device current), so make that first call
+ * before any stream capture.  All calls on a device share the array and it
+ * keeps the last call's contents: calls that overlap on the GPU (unordered
+ * streams) race.  A device-side wait timeout of this call is recorded in the
+ * shared array, not in a caller workspace, so dfa_stream_status cannot report
+ * it; the call's outputs are then invalid.
+ */
+dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void* q, const void* k,
+                                const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, void* stream);
+
 /* Bytes of workspace that op needs for desc (0 on invalid arguments). */
 size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op);
 

@@ -428,6 +428,18 @@ size_t bwd_ws_bytes(const dfa_attn_desc& d)
 
 }  // namespace
 
+namespace dfa {
+// Record the calling thread's last-error text (used by other translation units).
+dfa_status set_error(dfa_status s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace dfa
+
 // ============================================================================
 // C ABI
 // ============================================================================

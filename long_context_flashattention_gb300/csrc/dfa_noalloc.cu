@@ -1,0 +1,88 @@
+// dfa_noalloc.cu -- dfa_attn_bwd_noalloc: the attention backward for callers
+// that cannot allocate device memory.
+//
+// dfa_attn_bwd needs scratch memory (an fp32 dQ accumulator, the per-row D
+// values and a status word) in a caller-supplied workspace.  Some callers have
+// no way to obtain one: code running where cudaMalloc is not allowed or not
+// wanted (a host callback, a plugin that only receives tensor pointers from
+// its framework, a latency-critical loop that forbids allocation after
+// start-up).  This entry point takes its scratch from a fixed array in device
+// memory that belongs to the library instead.
+//
+// The array is a file-scope __device__ variable of kNoAllocScratchBytes: every
+// GPU that loads the library holds it until the process exits.  Its device
+// address is looked up once per device (cudaGetSymbolAddress, with that
+// device current) on the first call made on that device; that first call
+// should therefore come before any stream capture.  Every call on a device
+// shares the one array, which keeps the last call's contents: calls that
+// overlap on the GPU (different streams, no ordering between them) race on it.
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dfa.h"
+
+namespace dfa {
+dfa_status set_error(dfa_status s, const char* fmt, ...);
+}
+
+static constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// device variable: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void* q,
+                                           const void* k, const void* v, const void* o,
+                                           const void* dout, const float* lse, void* dq,
+                                           void* dk, void* dv, void* stream)
+{
+    if (!desc)
+        return dfa::set_error(DFA_ERR_INVALID_ARG, "desc is NULL");
+    // scratch this problem needs: status word + fp32 dQ accumulator + D
+    const size_t rows = (size_t)(desc->B > 0 ? desc->B : 0) * (size_t)(desc->Hq > 0 ? desc->Hq : 0) *
+                        (size_t)(desc->N > 0 ? desc->N : 0);
+    const size_t need = kStatusBytes + align256(rows * (size_t)(desc->d > 0 ? desc->d : 0) * 4) +
+                        align256(rows * 4);
+    if (need > kNoAllocScratchBytes)
+        return dfa::set_error(DFA_ERR_WORKSPACE,
+                              "dfa_attn_bwd_noalloc: this problem needs %zu bytes of scratch "
+                              "(256 + B*Hq*N*(4d + 4), rounded), above the fixed %zu",
+                              need, kNoAllocScratchBytes);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: no usable current device");
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!g_scratch_ptr[dev]) {
+            void* ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr)
+                return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: scratch lookup: %s",
+                                      cudaGetErrorString(e));
+            g_scratch_ptr[dev] = ptr;
+        }
+        scratch = g_scratch_ptr[dev];
+    }
+    // The status word must start at zero; the dQ accumulator and D are
+    // rewritten by the backward's own preprocess step.
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, kStatusBytes, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: %s", cudaGetErrorString(e));
+    return dfa_attn_bwd(desc, q, k, v, o, dout, lse, dq, dk, dv, scratch, kNoAllocScratchBytes,
+                        stream);
+}

@@ -72,6 +72,7 @@ def lib():
         sigs = {
             "dfa_attn_fwd": (i32, [D, vp, vp, vp, vp, vp, vp, sz, vp]),
             "dfa_attn_bwd": (i32, [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "dfa_attn_bwd_noalloc": (i32, [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "dfa_chunk_fwd": (i32, [D, ctypes.POINTER(ChunkPair), i64, i64, vp, vp, vp, vp, vp,
                                     vp, sz, vp]),
             "dfa_chunk_bwd": (i32, [D, ctypes.POINTER(ChunkPair), i64, i64, vp, vp, vp, vp, vp,
@@ -185,6 +186,21 @@ def attn_bwd(q, k, v, o, dout, lse, causal=True, scale=None, P=1, partition="con
     _check(lib().dfa_attn_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
                               _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                               ws.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, causal=True, scale=None, P=1,
+                     partition="contiguous", stripe=1, dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd without a workspace: the library's fixed 64 MiB device scratch is
+    used instead (for callers that cannot allocate; calls must not overlap)."""
+    _need_cuda(q, k, v, o, dout, lse)
+    desc = desc_for(q, k, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().dfa_attn_bwd_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      _stream(stream)))
     return dq, dk, dv
 
 
