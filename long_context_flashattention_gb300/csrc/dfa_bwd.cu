@@ -224,44 +224,57 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (warp 8, lane 0)
+// MMA issuer (warp 12, lane 0)
 // ---------------------------------------------------------------------------
+// Step m may start once its Q/dO stage has landed and the dQ^T of step m - 2,
+// which lives in the same TMEM buffer, has been drained.
+template <int D>
+__device__ __forceinline__ bool sdp_ready(uint64_t* bar, uint32_t m, const WaitCtx& w)
+{
+    using C = Cfg<D>;
+    if (!mbar_wait(&bar[C::QFULL + m % C::kQStages], (m / C::kQStages) & 1, w, 61))
+        return false;
+    if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + (m & 1)], ((m >> 1) - 1) & 1, w, 62))
+        return false;
+    tc_fence_after();
+    return true;
+}
+
+// S^T = K Q^T and dP^T = V dO^T of step m into TMEM buffer m & 1.
+template <int D>
+__device__ __forceinline__ void issue_sdp(uint32_t tmem, uint32_t m, uint64_t dKk, uint64_t dVk,
+                                          uint64_t dQk, uint64_t dDOk)
+{
+    using C = Cfg<D>;
+    constexpr uint32_t idSt = idesc_bf16_f32(128, BQ, false, false);
+    const uint32_t qst = (m % C::kQStages) * C::kQTile;
+    const int b = m & 1;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t qa = qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+        mma_ss(tmem + C::cS(b), sdesc_add(dKk, ka), sdesc_add(dQk, qa), idSt, kk > 0);
+        mma_ss(tmem + C::cDP(b), sdesc_add(dVk, ka), sdesc_add(dDOk, qa), idSt, kk > 0);
+    }
+}
 template <int D>
 __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh, const WaitCtx& w)
 {
     using C = Cfg<D>;
     uint64_t* bar = sh.bar;
     const uint32_t tmem = sh.tmem;
-    constexpr uint32_t idSt = idesc_bf16_f32(128, BQ, false, false);
     constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
     constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, true, true);
-    const uint32_t sK = smem_u32(sh.smem + C::kK), sV = smem_u32(sh.smem + C::kV);
-    const uint32_t sQ = smem_u32(sh.smem + C::kQ0), sDO = smem_u32(sh.smem + C::kDO0);
-    const uint32_t sDs0 = smem_u32(sh.smem + C::kDs0);
+    // base descriptors (K-major views for S^T / dP^T, MN-major for the rest)
+    const uint64_t dKk = sdesc_sw128(smem_u32(sh.smem + C::kK), 16, 1024);
+    const uint64_t dVk = sdesc_sw128(smem_u32(sh.smem + C::kV), 16, 1024);
+    const uint64_t dQk = sdesc_sw128(smem_u32(sh.smem + C::kQ0), 16, 1024);
+    const uint64_t dDOk = sdesc_sw128(smem_u32(sh.smem + C::kDO0), 16, 1024);
+    const uint64_t dQm = sdesc_sw128(smem_u32(sh.smem + C::kQ0), BQ * 128, 1024);
+    const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO0), BQ * 128, 1024);
+    const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
+    const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs0), 16384, 1024);
     uint32_t uc = 0, n = 0;
-
-    // S^T = K Q^T and dP^T = V dO^T of step m into buffer m & 1
-    auto issue_sdp = [&](uint32_t m) -> bool {
-        const int st = m % C::kQStages;
-        const int b = m & 1;
-        if (!mbar_wait(&bar[C::QFULL + st], (m / C::kQStages) & 1, w, 61))
-            return false;
-        // buffer b last held the dQ^T of step m - 2: the drain must have read it
-        if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + b], ((m >> 1) - 1) & 1, w, 62))
-            return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint32_t qa = st * C::kQTile + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::cS(b), sdesc_sw128(sK + ka, 16, 1024), sdesc_sw128(sQ + qa, 16, 1024),
-                   idSt, kk > 0);
-            mma_ss(tmem + C::cDP(b), sdesc_sw128(sV + ka, 16, 1024),
-                   sdesc_sw128(sDO + qa, 16, 1024), idSt, kk > 0);
-        }
-        tc_commit(&bar[C::SFULL + b]);
-        return true;
-    };
 
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
@@ -272,14 +285,20 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
             return;
         ++uc;
         tc_fence_after();
-        if (!issue_sdp(n))
+        if (!sdp_ready<D>(bar, n, w))
             return;
+        issue_sdp<D>(sh.tmem, n, dKk, dVk, dQk, dDOk);
+        tc_commit(&bar[C::SFULL + (n & 1)]);
         for (int it = 0; it < T; ++it, ++n) {
             const int st = n % C::kQStages;
             const int b = n & 1;
             const uint32_t ph = (n >> 1) & 1;
-            if (it + 1 < T && !issue_sdp(n + 1))
-                return;
+            if (it + 1 < T) {
+                if (!sdp_ready<D>(bar, n + 1, w))
+                    return;
+                issue_sdp<D>(sh.tmem, n + 1, dKk, dVk, dQk, dDOk);
+                tc_commit(&bar[C::SFULL + ((n + 1) & 1)]);
+            }
             // dV += P^T dO
             if (!mbar_wait(&bar[C::PFULL + b], ph, w, 63))
                 return;
@@ -287,7 +306,7 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDV, tmem + C::cS(b) + ptcol(kk),
-                       sdesc_sw128(sDO + st * C::kQTile + kk * 2048, BQ * 128, 1024), idKV,
+                       sdesc_add(dDOm, st * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             // dK += dS^T Q
             if (!mbar_wait(&bar[C::DSFULL + b], ph, w, 64))
@@ -296,15 +315,14 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDK, tmem + C::cDP(b) + ptcol(kk),
-                       sdesc_sw128(sQ + st * C::kQTile + kk * 2048, BQ * 128, 1024), idKV,
+                       sdesc_add(dQm, st * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&bar[C::QEMPTY + st]);
             // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the S^T columns of b
-            const uint32_t sDs = sDs0 + b * C::kDsBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tmem + C::cS(b), sdesc_sw128(sK + kk * 2048, 16384, 1024),
-                       sdesc_sw128(sDs + kk * 2048, 16384, 1024), idQ, kk > 0);
+                mma_ss(tmem + C::cS(b), sdesc_add(dKm, kk * 2048),
+                       sdesc_add(dDsm, b * C::kDsBytes + kk * 2048), idQ, kk > 0);
             tc_commit(&bar[C::DQFULL + b]);
             tc_commit(&bar[C::DSEMPTY + b]);
         }

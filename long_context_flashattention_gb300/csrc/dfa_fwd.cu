@@ -89,6 +89,30 @@ __device__ __forceinline__ int32_t unit_tiles(const FwdParams& p, const Unit& un
     return t;
 }
 
+// S = Q K^T for one 128-row query tile (D/16 K steps of 16).
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tS, uint64_t dQ0, uint64_t dK0, uint32_t qoff,
+                                        uint32_t koff)
+{
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_ss(tS, sdesc_add(dQ0, qoff + off), sdesc_add(dK0, koff + off), idS, kk > 0);
+    }
+}
+
+// O += P V with P (bf16) in TMEM over the S columns, V MN-major in SMEM.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint64_t dV0, uint32_t voff,
+                                         bool acc)
+{
+    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tO, tP + kk * 8, sdesc_add(dV0, voff + kk * 2048), idO, (acc || kk > 0) ? 1u : 0u);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -197,30 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == 8) {
             // ------------------------------------------------------------- MMA issuer
             if (lane == 0) {
-                constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-                constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-                const uint32_t sQ = smem_u32(smem + C::kQ0);
-                const uint32_t sK = smem_u32(smem + C::kK0);
-                const uint32_t sV = smem_u32(smem + C::kV0);
+                // base descriptors; K steps and stages only advance the start address
+                const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::kQ0), 16, 1024);
+                const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::kK0), 16, 1024);
+                const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::kV0), 16384, 1024);
                 const uint32_t tS0 = tmem, tS1 = tmem + 128;
                 const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
                 uint32_t kc = 0, qc = 0, pc0 = 0, pc1 = 0;
-
-                auto issue_s = [&](uint32_t tS, uint32_t qoff, int ks) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tS, sdesc_sw128(sQ + qoff + off, 16, 1024),
-                               sdesc_sw128(sK + ks * C::kTile + off, 16, 1024), idS, kk > 0);
-                    }
-                };
-                auto issue_pv = [&](uint32_t tO, uint32_t tP, int vs, bool acc) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tO, tP + kk * 8,
-                               sdesc_sw128(sV + vs * C::kTile + kk * 2048, 16384, 1024), idO,
-                               (acc || kk > 0) ? 1u : 0u);
-                };
 
                 for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
                     Unit un = decode_unit(p.units, p.BH, kRowsPerUnit, u, false);
@@ -236,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(&bar[C::KFULL + ks], (kc / C::kStages) & 1, wctx, 21))
                             goto mma_done;
                         tc_fence_after();
-                        issue_s(tS0, 0, ks);
+                        issue_s<D>(tS0, dQ0, dK0, 0, ks * C::kTile);
                         tc_commit(&bar[C::SFULL + 0]);
-                        issue_s(tS1, C::kTile, ks);
+                        issue_s<D>(tS1, dQ0, dK0, C::kTile, ks * C::kTile);
                         tc_commit(&bar[C::SFULL + 1]);
                         tc_commit(&bar[C::KEMPTY + ks]);
                     }
@@ -252,23 +259,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             goto mma_done;
                         ++pc0;
                         tc_fence_after();
-                        issue_pv(tO0, tS0, vs, it > 0);
+                        issue_pv<D>(tO0, tS0, dV0, vs * C::kTile, it > 0);
                         if (has_next) {
                             if (!mbar_wait(&bar[C::KFULL + ks2], ((kc + 1) / C::kStages) & 1, wctx,
                                            24))
                                 goto mma_done;
                             tc_fence_after();
-                            issue_s(tS0, 0, ks2);
+                            issue_s<D>(tS0, dQ0, dK0, 0, ks2 * C::kTile);
                             tc_commit(&bar[C::SFULL + 0]);
                         }
                         if (!mbar_wait(&bar[C::PFULL + 1], pc1 & 1, wctx, 25))
                             goto mma_done;
                         ++pc1;
                         tc_fence_after();
-                        issue_pv(tO1, tS1, vs, it > 0);
+                        issue_pv<D>(tO1, tS1, dV0, vs * C::kTile, it > 0);
                         tc_commit(&bar[C::VEMPTY + vs]);
                         if (has_next) {
-                            issue_s(tS1, C::kTile, ks2);
+                            issue_s<D>(tS1, dQ0, dK0, C::kTile, ks2 * C::kTile);
                             tc_commit(&bar[C::SFULL + 1]);
                             tc_commit(&bar[C::KEMPTY + ks2]);
                         }
@@ -334,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 128; ++i)
                                 sv[i] = (i < nv) ? sv[i] : -INFINITY;
                         }
-                        float mx = sv[0];
+                        // row max, two new values per 3-input max
+                        float mx = fmaxf(sv[0], sv[1]);
 #pragma unroll
-                        for (int i = 1; i < 128; ++i)
-                            mx = fmaxf(mx, sv[i]);
+                        for (int i = 2; i < 128; i += 2)
+                            mx = fmax3(mx, sv[i], sv[i + 1]);
                         const float m_new = fmaxf(m_ref, mx);
                         // Lazy rescale: keep the old reference max unless the
                         // row max grew by more than 2^8 in the exp2 domain.
@@ -365,16 +373,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
+                        const uint64_t c2x2 = f2pack(c2, c2), nmb2 = f2pack(-mb, -mb);
                         uint32_t pk[64];
-                        float lsum = 0.f;
+                        // two partial sums so that the packed adds are independent
+                        uint64_t sum2a = f2pack(0.f, 0.f), sum2b = f2pack(0.f, 0.f);
 #pragma unroll
                         for (int i = 0; i < 64; ++i) {
-                            const float a = ex2(fmaf(sv[2 * i], c2, -mb));
-                            const float b2 = ex2(fmaf(sv[2 * i + 1], c2, -mb));
-                            lsum += a + b2;
+                            float x0, x1;
+                            f2unpack(f2fma(f2pack(sv[2 * i], sv[2 * i + 1]), c2x2, nmb2), x0, x1);
+                            const float a = ex2(x0), b2 = ex2(x1);
+                            if (i & 1)
+                                sum2b = f2add(sum2b, f2pack(a, b2));
+                            else
+                                sum2a = f2add(sum2a, f2pack(a, b2));
                             pk[i] = pack_bf16x2(a, b2);
                         }
-                        l += lsum;
+                        float s0, s1, s2, s3;
+                        f2unpack(sum2a, s0, s1);
+                        f2unpack(sum2b, s2, s3);
+                        l += (s0 + s1) + (s2 + s3);
                         tmem_st32(tS + 0, pk);
                         tmem_st32(tS + 32, pk + 32);
                         tmem_st_wait();

@@ -200,14 +200,18 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
 }
 
 // D(tmem) (+)= A(smem desc) * B(smem desc)^T, bf16 in, fp32 accumulate.
+// The MMA reads only shared / tensor memory that the async proxy owns, so the
+// asm has no "memory" clobber: it stays ordered against the other volatile
+// asm (barrier waits, commits) without forcing the compiler to reload every
+// value it holds in memory after each issue, which keeps the single issuing
+// thread ahead of the tensor pipe.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // D(tmem) (+)= A(tmem) * B(smem desc).  A is M=128 lanes x K, two bf16 per column.
@@ -217,8 +221,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
@@ -231,6 +234,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            | ((b_mn_major ? 1u : 0u) << 16)        // B major
            | ((uint32_t)(N >> 3) << 17)            // N
            | ((uint32_t)(M >> 4) << 24);           // M
+}
+
+// A descriptor advanced by `bytes` (a multiple of 16) along its start address.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes)
+{
+    return desc + (uint64_t)(bytes >> 4);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.  saddr must lie in a
@@ -357,6 +366,13 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ float lg2(float x)
