@@ -110,19 +110,42 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def kernel_traffic(kernel_file: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
-    p = os.path.join(ROOT, "profiles", kernel_file)
+KERNEL_SOURCES = {
+    "attn_bwd_kernel": ("dfa_bwd.cu", "dfa_ptx.cuh", "dfa_params.h", "dfa_api.cu"),
+    "attn_fwd_kernel": ("dfa_fwd.cu", "dfa_ptx.cuh", "dfa_params.h", "dfa_api.cu"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 over the sources that shape a
+    kernel's launch (its .cu, the PTX helpers, the parameter structs and the
+    host code that orders its work units), in a fixed order."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "long_context_flashattention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(summary: str, kernel: str):
+    """DRAM bytes (read + write) per launch from a committed ncu summary
+    (`key: value` lines), or None unless it was taken on the current sources
+    of the kernel."""
+    p = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(p):
         return None
+    fields = {}
     with open(p) as f:
-        d = json.load(f)
-    with open(source, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    if d.get("source_sha256_16") != h:
+        for line in f:
+            if ":" in line and not line.startswith(("#", "|", " ")):
+                key, _, val = line.partition(":")
+                fields[key.strip()] = val.strip().strip("`")
+    if fields.get("source_sha256_16") != source_hash(kernel):
         return None
-    return d.get("dram_bytes_per_launch_full_size")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ----------------------------------------------------------------------------
@@ -263,7 +286,6 @@ def run_gpu(args):
     fwd_tflops = w.flops_fwd / (fwd_call_ms * 1e-3) / 1e12
     peak_s = pk["bf16_tflops_sustained"]
     merge_gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
-    bwd_src = os.path.join(ROOT, "long_context_flashattention_gb300", "csrc", "dfa_bwd.cu")
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -293,7 +315,8 @@ def run_gpu(args):
             "bound": "tensor", "achieved": round(bwd_tflops, 2), "peak": peak_s,
             "unit": "TFLOP/s", "frac": round(bwd_tflops / peak_s, 4),
             "peak_source": f"{src} bf16_tflops_sustained",
-            "traffic": kernel_traffic("attn_bwd_kernel_llama7b_128k.json", bwd_src),
+            "traffic": kernel_traffic("attn_bwd_kernel_llama7b_128k_traffic.md",
+                                      "attn_bwd_kernel"),
         },
         "merge": {"kernel": "dfa::lse_merge_kernel", "k": P, "rows": rows,
                   "bytes": merge_bytes, "ms": round(merge_ms, 4),

@@ -34,10 +34,11 @@ namespace fwd {
 
 constexpr int kThreads = 384;      // three warpgroups
 // Launch: 384 threads x 168 registers = 64512.  The producer/MMA warpgroup
-// drops to 40, the two math warpgroups rise to 232: 128 * (232 + 232 + 40)
+// drops to 120, the two math warpgroups rise to 192: 128 * (192 + 192 + 120)
 // = 64512, the launch's total.
 constexpr int kRegsMath = 192;
 constexpr int kRegsCtl = 120;
+static_assert(2 * kRegsMath + kRegsCtl == 3 * 168, "register budget");
 constexpr int kRowsPerUnit = 256;  // two 128-row query tiles
 constexpr float kRescaleLog2 = 8.0f;
 
