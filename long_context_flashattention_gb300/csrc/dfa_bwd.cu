@@ -15,14 +15,15 @@
 // tile ("step") of every query head of its group.  Key rows sit on TMEM lanes,
 // so dK and dV accumulate in TMEM for the whole unit.
 //   warp 13     producer: K, V once per unit (TMA); per step the Q and dO
-//               tiles (TMA) and the LSE / D values into a 3-stage ring.
-//   warp 12     MMA issuer.  Per step n, with TMEM buffer b = n & 1:
-//                 S^T = K Q^T and dP^T = V dO^T of step n+1 are issued
-//                 BEFORE the step-n products, so the tensor core computes
-//                 them while the softmax warps work on step n;
-//                 dV += P^T dO, dK += dS^T Q (A operand read from TMEM);
-//                 dQ^T = K^T dS^T into the S^T columns of buffer b (their P^T
-//                 has been consumed by dV).
+//               tiles (TMA) and the LSE / D values (cp.async) into a 3-stage
+//               ring, all completing on one barrier per stage.
+//   warp 14     issues S^T = K Q^T and dP^T = V dO^T of each step into a
+//               double-buffered TMEM pair, up to two steps ahead, so that
+//               they overlap the softmax warps' work on the previous step.
+//   warp 12     issues dV += P^T dO and dK += dS^T Q (A operand read from
+//               TMEM), then dQ^T = K^T dS^T into the dP^T columns (their
+//               dS^T has been consumed by dK).  Two issuing threads keep the
+//               tensor core fed while either one waits on a barrier.
 //   warps 0-7   two warpgroups, one thread per key row, each on 32 of the
 //               step's 64 query columns: P^T = exp2(S^T c - LSE log2 e),
 //               dS^T = P^T (dP^T - D) (packed f32x2 arithmetic), written as
@@ -31,10 +32,10 @@
 //               stores dK (scaled), the second dV.
 //   warps 8-11  drain each step's dQ^T tile from TMEM into the fp32 dQ
 //               accumulator with coalesced atomics.
-//   warps 14-15 give their registers to the other warpgroups.
+//   warp 15    gives its registers to the other warpgroups.
 // TMEM columns: dK [0,d) dV [d,2d), then per buffer b: S^T [2d+128b, +64),
-// dP^T [2d+128b+64, +64).  d = 64 uses the same path: the K tile is padded
-// to 128 columns with zeros so that dQ^T has 128 lanes.
+// dP^T (later dQ^T) [2d+128b+64, +64).  d = 64 uses the same path: the K
+// tile is padded to 128 columns with zeros so that dQ^T has 128 lanes.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,7 +55,7 @@ constexpr int kRegsSoft = 152;
 constexpr int kRegsDrain = 88;
 constexpr int kRegsCtl = 120;
 static_assert(2 * kRegsSoft + kRegsDrain + kRegsCtl == 512, "register budget");
-constexpr int kWarpMma = 12, kWarpProducer = 13;
+constexpr int kWarpMma = 12, kWarpProducer = 13, kWarpMmaS = 14;
 constexpr int kKvRows = 128;
 constexpr int BQ = 64;  // query rows per step
 
@@ -73,10 +74,13 @@ struct Cfg {
     static constexpr int kLse0 = kDs0 + 2 * kDsBytes;      // kQStages x BQ floats
     static constexpr int kDel0 = kLse0 + kQStages * BQ * 4;
     static constexpr int kBar = kDel0 + kQStages * BQ * 4;
+    // SFULL: S^T, dP^T of a step computed; PFULL: its P^T and dS^T written
+    // (TMEM and SMEM); DQFULL: its dQ^T computed, which also frees its dS^T
+    // SMEM tile; DQEMPTY: dQ^T read out of TMEM.
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
                          SFULL = QEMPTY + kQStages,  // two of each from here
-        PFULL = SFULL + 2, DSFULL = PFULL + 2, DSEMPTY = DSFULL + 2, DQFULL = DSEMPTY + 2,
-                         DQEMPTY = DQFULL + 2, DKVFULL = DQEMPTY + 2, NBAR = DKVFULL + 1;
+        PFULL = SFULL + 2, DQFULL = PFULL + 2, DQEMPTY = DQFULL + 2, DKVFULL = DQEMPTY + 2,
+                         NBAR = DKVFULL + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t cDK = 0, cDV = D;
     __host__ __device__ static constexpr uint32_t cS(int b) { return 2 * D + 128 * b; }
@@ -188,23 +192,21 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
                     __syncwarp();
                     if (*sh.abort_flag)
                         return;
-                    // -LSE in log2 units (a row without keys gives -inf, so that
-                    // P = 0; so do rows past the chunk) and -D
+                    // LSE and D of the step's rows, copied asynchronously so that
+                    // the producer never waits on them; rows past the chunk read
+                    // as 0 (their P is masked).  Completion joins the Q/dO
+                    // barrier, whose phase cannot end before lane 0 arrives.
                     const int32_t m0 = i * BQ;
                     const size_t rbase = (size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q + m0;
-                    float* sl = (float*)(smem + C::kLse0 + st * BQ * 4);
-                    float* sd = (float*)(smem + C::kDel0 + st * BQ * 4);
+                    const uint32_t sl = smem_u32(smem + C::kLse0 + st * BQ * 4);
+                    const uint32_t sd = smem_u32(smem + C::kDel0 + st * BQ * 4);
 #pragma unroll
                     for (int c = lane; c < BQ; c += 32) {
-                        float nl = -INFINITY, nd = 0.f;
-                        if (m0 + c < p.chunk_q) {
-                            const float lv = p.lse[rbase + c];
-                            nl = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
-                            nd = -p.delta[rbase + c];
-                        }
-                        sl[c] = nl;
-                        sd[c] = nd;
+                        const bool in = m0 + c < p.chunk_q;
+                        cp_async_4(sl + 4 * c, in ? p.lse + rbase + c : p.lse, in ? 4u : 0u);
+                        cp_async_4(sd + 4 * c, in ? p.delta + rbase + c : p.delta, in ? 4u : 0u);
                     }
+                    cp_async_mbar_arrive(&bar[C::QFULL + st]);
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&bar[C::QFULL + st], 2 * C::kQTile);
@@ -226,56 +228,32 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 // ---------------------------------------------------------------------------
 // MMA issuer (warp 12, lane 0)
 // ---------------------------------------------------------------------------
-// Step m may start once its Q/dO stage has landed and the dQ^T of step m - 2,
-// which lives in the same TMEM buffer, has been drained.
+// Two threads issue the MMAs, so that one thread's barrier waits (each of
+// which would otherwise leave the tensor core idle: it queues only one or
+// two instructions) are covered by the other's issues.  Every dependency
+// between them goes through a completion barrier, never through issue order.
+//
+// Warp 14 (issue_products), per step m, buffer b = m & 1:
+//   S^T(m) = K Q(m)^T    once Q(m) has landed and dV / dK of step m-2 (which
+//                        read P^T / dS^T from buffer b) are complete;
+//   dP^T(m) = V dO(m)^T  once the dQ^T of step m-2 has left buffer b.
+// Warp 12 (issue_grads), per step n, buffer b = n & 1:
+//   dV += P^T(n) dO(n), dK += dS^T(n) Q(n)   (A operand read from TMEM)
+//                        once the softmax warps have written P^T and dS^T;
+//   dQ^T(n) = K^T dS^T(n) into the dP^T columns of b.
 template <int D>
-__device__ __forceinline__ bool sdp_ready(uint64_t* bar, uint32_t m, const WaitCtx& w)
-{
-    using C = Cfg<D>;
-    if (!mbar_wait(&bar[C::QFULL + m % C::kQStages], (m / C::kQStages) & 1, w, 61))
-        return false;
-    if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + (m & 1)], ((m >> 1) - 1) & 1, w, 62))
-        return false;
-    tc_fence_after();
-    return true;
-}
-
-// S^T = K Q^T and dP^T = V dO^T of step m into TMEM buffer m & 1.
-template <int D>
-__device__ __forceinline__ void issue_sdp(uint32_t tmem, uint32_t m, uint64_t dKk, uint64_t dVk,
-                                          uint64_t dQk, uint64_t dDOk)
-{
-    using C = Cfg<D>;
-    constexpr uint32_t idSt = idesc_bf16_f32(128, BQ, false, false);
-    const uint32_t qst = (m % C::kQStages) * C::kQTile;
-    const int b = m & 1;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t qa = qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-        mma_ss(tmem + C::cS(b), sdesc_add(dKk, ka), sdesc_add(dQk, qa), idSt, kk > 0);
-        mma_ss(tmem + C::cDP(b), sdesc_add(dVk, ka), sdesc_add(dDOk, qa), idSt, kk > 0);
-    }
-}
-template <int D>
-__device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh, const WaitCtx& w)
+__device__ __forceinline__ void issue_products(const BwdParams& p, const Shared& sh,
+                                               const WaitCtx& w)
 {
     using C = Cfg<D>;
     uint64_t* bar = sh.bar;
     const uint32_t tmem = sh.tmem;
-    constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
-    constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, true, true);
-    // base descriptors (K-major views for S^T / dP^T, MN-major for the rest)
+    constexpr uint32_t idSt = idesc_bf16_f32(128, BQ, false, false);
     const uint64_t dKk = sdesc_sw128(smem_u32(sh.smem + C::kK), 16, 1024);
     const uint64_t dVk = sdesc_sw128(smem_u32(sh.smem + C::kV), 16, 1024);
     const uint64_t dQk = sdesc_sw128(smem_u32(sh.smem + C::kQ0), 16, 1024);
     const uint64_t dDOk = sdesc_sw128(smem_u32(sh.smem + C::kDO0), 16, 1024);
-    const uint64_t dQm = sdesc_sw128(smem_u32(sh.smem + C::kQ0), BQ * 128, 1024);
-    const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO0), BQ * 128, 1024);
-    const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
-    const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs0), 16384, 1024);
-    uint32_t uc = 0, n = 0;
-
+    uint32_t uc = 0, m = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
         const int T = unit_steps(p, un);
@@ -284,48 +262,84 @@ __device__ __forceinline__ void mma_issuer(const BwdParams& p, const Shared& sh,
         if (!mbar_wait(&bar[C::KVFULL], uc & 1, w, 60))
             return;
         ++uc;
-        tc_fence_after();
-        if (!sdp_ready<D>(bar, n, w))
+        for (int it = 0; it < T; ++it, ++m) {
+            const int b = m & 1;
+            const uint32_t qst = (m % C::kQStages) * C::kQTile;
+            if (!mbar_wait(&bar[C::QFULL + m % C::kQStages], (m / C::kQStages) & 1, w, 61))
+                return;
+            if (m >= 2) {
+                const uint32_t o = m - 2;
+                if (!mbar_wait(&bar[C::QEMPTY + o % C::kQStages], (o / C::kQStages) & 1, w, 62))
+                    return;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + C::cS(b), sdesc_add(dKk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(dQk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
+                       kk > 0);
+            if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + b], ((m - 2) >> 1) & 1, w, 65))
+                return;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + C::cDP(b), sdesc_add(dVk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(dDOk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
+                       kk > 0);
+            tc_commit(&bar[C::SFULL + b]);
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh, const WaitCtx& w)
+{
+    using C = Cfg<D>;
+    uint64_t* bar = sh.bar;
+    const uint32_t tmem = sh.tmem;
+    constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, true, true);
+    const uint64_t dQm = sdesc_sw128(smem_u32(sh.smem + C::kQ0), BQ * 128, 1024);
+    const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO0), BQ * 128, 1024);
+    const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
+    const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs0), 16384, 1024);
+    uint32_t uc = 0, n = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        const int T = unit_steps(p, un);
+        if (T == 0)
+            continue;
+        if (!mbar_wait(&bar[C::KVFULL], uc & 1, w, 66))
             return;
-        issue_sdp<D>(sh.tmem, n, dKk, dVk, dQk, dDOk);
-        tc_commit(&bar[C::SFULL + (n & 1)]);
+        ++uc;
         for (int it = 0; it < T; ++it, ++n) {
             const int st = n % C::kQStages;
             const int b = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            if (it + 1 < T) {
-                if (!sdp_ready<D>(bar, n + 1, w))
-                    return;
-                issue_sdp<D>(sh.tmem, n + 1, dKk, dVk, dQk, dDOk);
-                tc_commit(&bar[C::SFULL + ((n + 1) & 1)]);
-            }
-            // dV += P^T dO
-            if (!mbar_wait(&bar[C::PFULL + b], ph, w, 63))
+            if (!mbar_wait(&bar[C::PFULL + b], (n >> 1) & 1, w, 63))
                 return;
             tc_fence_after();
+            // dV += P^T dO
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDV, tmem + C::cS(b) + ptcol(kk),
                        sdesc_add(dDOm, st * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             // dK += dS^T Q
-            if (!mbar_wait(&bar[C::DSFULL + b], ph, w, 64))
-                return;
-            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDK, tmem + C::cDP(b) + ptcol(kk),
                        sdesc_add(dQm, st * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&bar[C::QEMPTY + st]);
-            // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the S^T columns of b
+            // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the dP^T columns of b
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tmem + C::cS(b), sdesc_add(dKm, kk * 2048),
+                mma_ss(tmem + C::cDP(b), sdesc_add(dKm, kk * 2048),
                        sdesc_add(dDsm, b * C::kDsBytes + kk * 2048), idQ, kk > 0);
             tc_commit(&bar[C::DQFULL + b]);
-            tc_commit(&bar[C::DSEMPTY + b]);
         }
+        // all of the unit's MMAs are complete once these land: the S^T / dP^T
+        // of its last step completed before its softmax, hence before its dV
         tc_commit(&bar[C::DKVFULL]);
         tc_commit(&bar[C::KVEMPTY]);
     }
@@ -347,6 +361,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     const int r = (warp & 3) * 32 + lane;    // key row inside the unit tile (TMEM lane)
     const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
+    const uint64_t nlog2e = f2pack(-1.4426950408889634f, -1.4426950408889634f);
+    const uint64_t neg1 = f2pack(-1.f, -1.f);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
@@ -384,13 +400,15 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         uint32_t pp[16], dd[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            // two query columns 2j, 2j+1 at a time (f32x2)
-                            const uint64_t nl = *(const uint64_t*)(sl + 2 * j);
-                            const uint64_t nd = *(const uint64_t*)(sd + 2 * j);
+                            // two query columns 2j, 2j+1 at a time (f32x2):
+                            // P = exp2(S c - LSE log2 e).  A row without keys
+                            // (LSE = -inf) is never visible, so its P is masked.
+                            const uint64_t lp = *(const uint64_t*)(sl + 2 * j);
+                            const uint64_t dp = *(const uint64_t*)(sd + 2 * j);
                             float a0, a1;
                             f2unpack(f2fma(f2pack(__uint_as_float(sr[2 * j]),
                                                   __uint_as_float(sr[2 * j + 1])),
-                                           c2x2, nl),
+                                           c2x2, f2mul(lp, nlog2e)),
                                      a0, a1);
                             float p0 = ex2(a0), p1 = ex2(a1);
                             if (!full) {
@@ -401,9 +419,9 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                             pp[j] = pack_bf16x2(p0, p1);
                             float d0, d1;
                             f2unpack(f2mul(f2pack(p0, p1),
-                                           f2add(f2pack(__uint_as_float(dr[2 * j]),
-                                                        __uint_as_float(dr[2 * j + 1])),
-                                                 nd)),
+                                           f2fma(dp, neg1,
+                                                 f2pack(__uint_as_float(dr[2 * j]),
+                                                        __uint_as_float(dr[2 * j + 1])))),
                                      d0, d1);
                             dd[j] = pack_bf16x2(d0, d1);
                         }
@@ -412,7 +430,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         tmem_st16(tl + C::cS(b) + 32 * h, pp);
                         tmem_st16(tl + C::cDP(b) + 32 * h, dd);
                         // the dQ MMA of step n - 2 has read dS^T buffer b
-                        if (n >= 2 && !mbar_wait(&bar[C::DSEMPTY + b], ((n >> 1) - 1) & 1, w, 72))
+                        if (n >= 2 && !mbar_wait(&bar[C::DQFULL + b], ((n >> 1) - 1) & 1, w, 72))
                             return;
                         uint8_t* dsb = sh.smem + C::kDs0 + b * C::kDsBytes;
 #pragma unroll
@@ -424,7 +442,6 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(&bar[C::PFULL + b]);
-                        mbar_arrive(&bar[C::DSFULL + b]);
                     }
                 }
             }
@@ -513,8 +530,8 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
                         return;
                     tc_fence_after();
                     uint32_t v[64];
-                    tmem_ld32(tl + C::cS(b), v);
-                    tmem_ld32(tl + C::cS(b) + 32, v + 32);
+                    tmem_ld32(tl + C::cDP(b), v);
+                    tmem_ld32(tl + C::cDP(b) + 32, v + 32);
                     tmem_ld_wait();
                     tmem_reg_fence32(v);
                     tmem_reg_fence32(v + 32);
@@ -568,8 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar[C::SFULL + b], 1);
             mbar_init(&bar[C::PFULL + b], 256);
-            mbar_init(&bar[C::DSFULL + b], 256);
-            mbar_init(&bar[C::DSEMPTY + b], 1);
             mbar_init(&bar[C::DQFULL + b], 1);
             mbar_init(&bar[C::DQEMPTY + b], 128);
         }
@@ -603,7 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (warp == kWarpMma && lane == 0) {
-            mma_issuer<D>(p, sh, wctx);
+            issue_grads<D>(p, sh, wctx);
+        } else if (warp == kWarpMmaS && lane == 0) {
+            issue_products<D>(p, sh, wctx);
         }
     } else if (warp >= 8) {
         reg_dealloc<kRegsDrain>();

@@ -152,6 +152,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy; src_bytes = 0 stores a zero
+// without reading `src` (which must still be a valid address).
+__device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// The barrier's current phase also waits for every cp.async this thread has
+// issued so far (the arrival is counted in advance, so the barrier's expected
+// count is unchanged).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
