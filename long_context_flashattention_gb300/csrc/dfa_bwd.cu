@@ -74,13 +74,14 @@ struct Cfg {
     static constexpr int kLse0 = kDs0 + 2 * kDsBytes;      // kQStages x BQ floats
     static constexpr int kDel0 = kLse0 + kQStages * BQ * 4;
     static constexpr int kBar = kDel0 + kQStages * BQ * 4;
-    // SFULL: S^T, dP^T of a step computed; PFULL: its P^T and dS^T written
-    // (TMEM and SMEM); DQFULL: its dQ^T computed, which also frees its dS^T
-    // SMEM tile; DQEMPTY: dQ^T read out of TMEM.
+    // SFULL: S^T, dP^T of a step computed; PREADY: its P^T written to TMEM;
+    // DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its dQ^T computed,
+    // hence also its dV and dK (issued before it by the same thread), which
+    // frees its P^T / dS^T; DQEMPTY: dQ^T read out of TMEM.
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
                          SFULL = QEMPTY + kQStages,  // two of each from here
-        PFULL = SFULL + 2, DQFULL = PFULL + 2, DQEMPTY = DQFULL + 2, DKVFULL = DQEMPTY + 2,
-                         NBAR = DKVFULL + 1;
+        PREADY = SFULL + 2, DSREADY = PREADY + 2, DQFULL = DSREADY + 2, DQEMPTY = DQFULL + 2,
+                         DKVFULL = DQEMPTY + 2, NBAR = DKVFULL + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t cDK = 0, cDV = D;
     __host__ __device__ static constexpr uint32_t cS(int b) { return 2 * D + 128 * b; }
@@ -234,12 +235,14 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 // between them goes through a completion barrier, never through issue order.
 //
 // Warp 14 (issue_products), per step m, buffer b = m & 1:
-//   S^T(m) = K Q(m)^T    once Q(m) has landed and dV / dK of step m-2 (which
-//                        read P^T / dS^T from buffer b) are complete;
+//   S^T(m) = K Q(m)^T    once Q(m) has landed and the products of step m-2
+//                        are complete (its dQ^T last), so that S^T(m) queues
+//                        behind dK / dQ^T(m-2), which lie on the critical
+//                        path, and runs while their dQ^T is drained;
 //   dP^T(m) = V dO(m)^T  once the dQ^T of step m-2 has left buffer b.
 // Warp 12 (issue_grads), per step n, buffer b = n & 1:
-//   dV += P^T(n) dO(n), dK += dS^T(n) Q(n)   (A operand read from TMEM)
-//                        once the softmax warps have written P^T and dS^T;
+//   dV += P^T(n) dO(n)   once the softmax warps have written P^T;
+//   dK += dS^T(n) Q(n)   once they have written dS^T (A operands from TMEM);
 //   dQ^T(n) = K^T dS^T(n) into the dP^T columns of b.
 template <int D>
 __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared& sh,
@@ -267,11 +270,8 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
             const uint32_t qst = (m % C::kQStages) * C::kQTile;
             if (!mbar_wait(&bar[C::QFULL + m % C::kQStages], (m / C::kQStages) & 1, w, 61))
                 return;
-            if (m >= 2) {
-                const uint32_t o = m - 2;
-                if (!mbar_wait(&bar[C::QEMPTY + o % C::kQStages], (o / C::kQStages) & 1, w, 62))
-                    return;
-            }
+            if (m >= 2 && !mbar_wait(&bar[C::DQFULL + b], ((m - 2) >> 1) & 1, w, 62))
+                return;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -315,7 +315,8 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
         for (int it = 0; it < T; ++it, ++n) {
             const int st = n % C::kQStages;
             const int b = n & 1;
-            if (!mbar_wait(&bar[C::PFULL + b], (n >> 1) & 1, w, 63))
+            const uint32_t ph = (n >> 1) & 1;
+            if (!mbar_wait(&bar[C::PREADY + b], ph, w, 63))
                 return;
             tc_fence_after();
             // dV += P^T dO
@@ -325,6 +326,9 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
                        sdesc_add(dDOm, st * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             // dK += dS^T Q
+            if (!mbar_wait(&bar[C::DSREADY + b], ph, w, 64))
+                return;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDK, tmem + C::cDP(b) + ptcol(kk),
@@ -397,14 +401,15 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         tmem_ld_wait();
                         tmem_reg_fence32(sr);
                         tmem_reg_fence32(dr);
-                        uint32_t pp[16], dd[16];
+                        // phase 1: P^T, stored and signalled first so that dV can
+                        // start while dS^T is formed
+                        uint32_t pp[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             // two query columns 2j, 2j+1 at a time (f32x2):
                             // P = exp2(S c - LSE log2 e).  A row without keys
                             // (LSE = -inf) is never visible, so its P is masked.
                             const uint64_t lp = *(const uint64_t*)(sl + 2 * j);
-                            const uint64_t dp = *(const uint64_t*)(sd + 2 * j);
                             float a0, a1;
                             f2unpack(f2fma(f2pack(__uint_as_float(sr[2 * j]),
                                                   __uint_as_float(sr[2 * j + 1])),
@@ -416,18 +421,30 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                 p0 = (q >= qv && q < p.chunk_q) ? p0 : 0.f;
                                 p1 = (q + 1 >= qv && q + 1 < p.chunk_q) ? p1 : 0.f;
                             }
+                            sr[2 * j] = __float_as_uint(p0);
+                            sr[2 * j + 1] = __float_as_uint(p1);
                             pp[j] = pack_bf16x2(p0, p1);
+                        }
+                        // packed into the first 16 of this warpgroup's own 32 columns:
+                        // the other warpgroup may still be reading its half
+                        tmem_st16(tl + C::cS(b) + 32 * h, pp);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&bar[C::PREADY + b]);
+                        // phase 2: dS^T = P^T (dP^T - D)
+                        uint32_t dd[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint64_t dp = *(const uint64_t*)(sd + 2 * j);
                             float d0, d1;
-                            f2unpack(f2mul(f2pack(p0, p1),
+                            f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]),
+                                                  __uint_as_float(sr[2 * j + 1])),
                                            f2fma(dp, neg1,
                                                  f2pack(__uint_as_float(dr[2 * j]),
                                                         __uint_as_float(dr[2 * j + 1])))),
                                      d0, d1);
                             dd[j] = pack_bf16x2(d0, d1);
                         }
-                        // packed into the first 16 of this warpgroup's own 32 columns:
-                        // the other warpgroup may still be reading its half
-                        tmem_st16(tl + C::cS(b) + 32 * h, pp);
                         tmem_st16(tl + C::cDP(b) + 32 * h, dd);
                         // the dQ MMA of step n - 2 has read dS^T buffer b
                         if (n >= 2 && !mbar_wait(&bar[C::DQFULL + b], ((n >> 1) - 1) & 1, w, 72))
@@ -441,7 +458,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         tmem_st_wait();
                         fence_proxy_async_smem();
                         tc_fence_before();
-                        mbar_arrive(&bar[C::PFULL + b]);
+                        mbar_arrive(&bar[C::DSREADY + b]);
                     }
                 }
             }
@@ -584,7 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar[C::SFULL + b], 1);
-            mbar_init(&bar[C::PFULL + b], 256);
+            mbar_init(&bar[C::PREADY + b], 256);
+            mbar_init(&bar[C::DSREADY + b], 256);
             mbar_init(&bar[C::DQFULL + b], 1);
             mbar_init(&bar[C::DQEMPTY + b], 128);
         }
