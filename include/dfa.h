@@ -143,7 +143,9 @@ dfa_status dfa_attn_fwd(const dfa_attn_desc* desc, const void* q, const void* k,
  * heads of a key/value head).
  *   o [B,Hq,N,d] bf16 (the forward output), dout [B,Hq,N,d] bf16,
  *   lse [B,Hq,N] fp32 (the forward's);  dq [B,Hq,N,d], dk/dv [B,Hkv,N,d] bf16.
- *   ws: dfa_workspace_size(desc, DFA_OP_BWD) bytes (fp32 dQ accumulator and D).
+ *   ws: dfa_workspace_size(desc, DFA_OP_BWD) bytes: the fp32 dQ accumulator
+ *   and, per query row, 32-byte records of -LSE/scale and -D that the
+ *   kernel adds to S and dP on the tensor core.
  */
 dfa_status dfa_attn_bwd(const dfa_attn_desc* desc, const void* q, const void* k,
                         const void* v, const void* o, const void* dout, const float* lse,
@@ -175,6 +177,8 @@ dfa_status dfa_chunk_fwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, 
  * Accumulates (+=) into fp32 dq_acc [B,Hq,Lq,d], dk_acc / dv_acc
  * [B,Hkv,Lk,d]; the caller zeroes them before the first pair.  dq_acc and
  * dk_acc include the softmax scale.
+ *   ws: dfa_workspace_size(desc, DFA_OP_CHUNK_BWD) bytes with desc->N = Lq
+ *   (per query row the 32-byte -LSE/scale and -D records).
  */
 dfa_status dfa_chunk_bwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, int64_t Lq,
                          int64_t Lk, const void* q, const void* k, const void* v,
@@ -242,8 +246,9 @@ dfa_status dfa_partition_map(const dfa_attn_desc* desc, int32_t p, dfa_pos_map* 
  * Who needs it: code that has tensor pointers but no allocator it may use --
  * a plugin handed buffers by a host framework, a host callback, a loop that
  * forbids cudaMalloc after start-up.  dfa_attn_bwd needs a workspace of
- * 256 + B*Hq*N*(4d + 4) bytes (the fp32 dQ accumulator and D); here that
- * scratch is a fixed 64 MiB array in device memory owned by the library, held
+ * 256 + B*Hq*N*(4d + 64) bytes (the fp32 dQ accumulator and per-row
+ * records); here that scratch is a fixed 64 MiB array in device memory
+ * owned by the library, held
  * by every GPU that loads the library until the process exits.  Problems
  * whose scratch would exceed 64 MiB are rejected with DFA_ERR_WORKSPACE.
  *

@@ -260,6 +260,26 @@ dfa_status make_tmap(CUtensorMap* out, const void* ptr, int64_t slices, int64_t 
     return DFA_OK;
 }
 
+// The backward's per-row records: [slices, rows, 16] bf16 (32 bytes a row),
+// loaded 64 rows at a time with a 32-byte swizzle.
+dfa_status make_tmap_aug(CUtensorMap* out, const void* ptr, int64_t slices, int64_t rows,
+                         int box_rows, const char* name)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(DFA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)slices};
+    cuuint64_t strides[2] = {(cuuint64_t)kAugRowBytes, (cuuint64_t)rows * kAugRowBytes};
+    cuuint32_t box[3] = {16, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DFA_ERR_CUDA, "tensor map for %s failed (CUresult %d)", name, (int)r);
+    return DFA_OK;
+}
+
 DevStatus* status_word(void* ws) { return reinterpret_cast<DevStatus*>(ws); }
 
 dfa_status check_ws(void* ws, size_t have, size_t need)
@@ -333,9 +353,9 @@ dfa_status run_fwd(const dfa_attn_desc& d, const Layout& lay, const void* q, con
 }
 
 dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q, const void* k,
-                        const void* v, const void* dout, const float* lse, const float* delta,
-                        float* dq_acc, void* dk, void* dv, int dkv_mode, void* ws,
-                        cudaStream_t stream)
+                        const void* v, const void* dout, const void* aug_lse,
+                        const void* aug_delta, float* dq_acc, void* dk, void* dv, int dkv_mode,
+                        void* ws, cudaStream_t stream)
 {
     const int64_t Lq = lay.chunk_q * (int64_t)lay.qmaps.size();
     const int64_t Lk = lay.chunk_k * (int64_t)lay.kmaps.size();
@@ -362,8 +382,6 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
         p.qmap[i] = to_dev(lay.qmaps[i]);
     for (size_t i = 0; i < lay.kmaps.size(); ++i)
         p.kmap[i] = to_dev(lay.kmaps[i]);
-    p.lse = lse;
-    p.delta = delta;
     p.dq_acc = dq_acc;
     p.dk = dk;
     p.dv = dv;
@@ -372,10 +390,14 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     if (p.total_units == 0)
         return DFA_OK;
     const int bq = bwd_query_rows_per_step();
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tal, tad;
     dfa_status s;
     const int64_t BHq = (int64_t)d.B * d.Hq, BHkv = (int64_t)d.B * d.Hkv;
     if ((s = make_tmap(&tq, q, BHq, Lq, d.d, bq, "q")) != DFA_OK)
+        return s;
+    if ((s = make_tmap_aug(&tal, aug_lse, BHq, Lq, bq, "LSE records")) != DFA_OK)
+        return s;
+    if ((s = make_tmap_aug(&tad, aug_delta, BHq, Lq, bq, "D records")) != DFA_OK)
         return s;
     if ((s = make_tmap(&tdo, dout, BHq, Lq, d.d, bq, "dout")) != DFA_OK)
         return s;
@@ -384,7 +406,7 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     if ((s = make_tmap(&tv, v, BHkv, Lk, d.d, 128, "v")) != DFA_OK)
         return s;
     const int grid = std::min(p.total_units, num_sms());
-    cudaError_t e = launch_attn_bwd(d.d, tq, tk, tv, tdo, p, grid, stream);
+    cudaError_t e = launch_attn_bwd(d.d, tq, tk, tv, tdo, tal, tad, p, grid, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "attention backward launch");
     return DFA_OK;
@@ -420,10 +442,12 @@ dfa_status check_ptrs(std::initializer_list<const void*> ps)
     return DFA_OK;
 }
 
+// Backward workspace: status word, fp32 dQ accumulator, -LSE/scale and -D
+// records (32 bytes a row each).
 size_t bwd_ws_bytes(const dfa_attn_desc& d)
 {
     const size_t rows = (size_t)d.B * d.Hq * (size_t)d.N;
-    return kStatusBytes + align256(rows * d.d * 4) + align256(rows * 4);
+    return kStatusBytes + align256(rows * d.d * 4) + 2 * align256(rows * kAugRowBytes);
 }
 
 }  // namespace
@@ -479,7 +503,8 @@ size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op)
     case DFA_OP_BWD:
         return bwd_ws_bytes(*desc);
     case DFA_OP_CHUNK_BWD:
-        return kStatusBytes + align256((size_t)desc->B * desc->Hq * (size_t)desc->N * 4);
+        return kStatusBytes +
+               2 * align256((size_t)desc->B * desc->Hq * (size_t)desc->N * kAugRowBytes);
     }
     return 0;
 }
@@ -557,14 +582,15 @@ dfa_status dfa_attn_bwd(const dfa_attn_desc* desc, const void* q, const void* k,
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t rows = (int64_t)desc->B * desc->Hq * desc->N;
     float* dq_acc = reinterpret_cast<float*>((char*)ws + kStatusBytes);
-    float* delta = reinterpret_cast<float*>((char*)ws + kStatusBytes +
-                                            align256((size_t)rows * desc->d * 4));
+    char* aug_lse = (char*)ws + kStatusBytes + align256((size_t)rows * desc->d * 4);
+    char* aug_delta = aug_lse + align256((size_t)rows * kAugRowBytes);
     const int sms = num_sms();
-    cudaError_t e = launch_bwd_preprocess(rows, desc->d, o, dout, delta, dq_acc, sms, st);
+    cudaError_t e = launch_bwd_preprocess(rows, desc->d, o, dout, nullptr, lse, desc->scale,
+                                          aug_lse, aug_delta, dq_acc, sms, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward preprocess launch");
-    s = run_bwd_main(*desc, whole_layout(*desc), q, k, v, dout, lse, delta, dq_acc, dk, dv, 0, ws,
-                     st);
+    s = run_bwd_main(*desc, whole_layout(*desc), q, k, v, dout, aug_lse, aug_delta, dq_acc, dk,
+                     dv, 0, ws, st);
     if (s != DFA_OK)
         return s;
     e = launch_f32_to_bf16(rows * desc->d, dq_acc, dq, sms, st);
@@ -594,28 +620,27 @@ dfa_status dfa_chunk_bwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, 
     if (!lse)
         return fail(DFA_ERR_INVALID_ARG, "lse is NULL");
     const size_t rows = (size_t)desc->B * desc->Hq * (size_t)Lq;
-    const size_t need = kStatusBytes + (delta ? 0 : align256(rows * 4));
+    const size_t need = kStatusBytes + 2 * align256(rows * kAugRowBytes);
     if ((s = check_ws(ws, ws_bytes, need)) != DFA_OK)
         return s;
     cudaStream_t st = (cudaStream_t)stream;
-    const float* dl = delta;
-    if (!dl) {
-        if ((s = check_ptrs({o})) != DFA_OK)
-            return s;
-        float* tmp = reinterpret_cast<float*>((char*)ws + kStatusBytes);
-        cudaError_t e = launch_bwd_preprocess((int64_t)rows, desc->d, o, dout, tmp, nullptr,
-                                              num_sms(), st);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "backward preprocess launch");
-        dl = tmp;
-    }
+    if (!delta && (s = check_ptrs({o})) != DFA_OK)
+        return s;
+    char* aug_lse = (char*)ws + kStatusBytes;
+    char* aug_delta = aug_lse + align256(rows * kAugRowBytes);
+    cudaError_t e = launch_bwd_preprocess((int64_t)rows, desc->d, delta ? nullptr : o, dout, delta,
+                                          lse, desc->scale, aug_lse, aug_delta, nullptr,
+                                          num_sms(), st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward preprocess launch");
     Layout lay;
     lay.qmaps.push_back(pair->q);
     lay.kmaps.push_back(pair->kv);
     lay.chunk_q = Lq;
     lay.chunk_k = Lk;
     lay.ring = 0;
-    return run_bwd_main(*desc, lay, q, k, v, dout, lse, dl, dq_acc, dk_acc, dv_acc, 1, ws, st);
+    return run_bwd_main(*desc, lay, q, k, v, dout, aug_lse, aug_delta, dq_acc, dk_acc, dv_acc, 1,
+                        ws, st);
 }
 
 dfa_status dfa_lse_merge(int64_t rows, int32_t d, int32_t k, const float* o_parts,

@@ -15,18 +15,22 @@
 // tile ("step") of every query head of its group.  Key rows sit on TMEM lanes,
 // so dK and dV accumulate in TMEM for the whole unit.
 //   warp 13     producer: K, V once per unit (TMA); per step the Q and dO
-//               tiles (TMA) and the LSE / D values (cp.async) into a 3-stage
-//               ring, all completing on one barrier per stage.
-//   warp 14     issues S^T = K Q^T and dP^T = V dO^T of each step into a
-//               double-buffered TMEM pair, up to two steps ahead, so that
-//               they overlap the softmax warps' work on the previous step.
+//               tiles and the rows' -LSE/scale and -D records (TMA) into a
+//               3-stage ring, all completing on one barrier per stage.
+//   warp 14     issues S^T = K Q^T - LSE/scale and dP^T = V dO^T - D of each
+//               step into a double-buffered TMEM pair, up to two steps ahead,
+//               so that they overlap the softmax warps' work on the previous
+//               step.  The row constants enter as one more K = 16 slice of
+//               each product: a ones tile against per-row records holding the
+//               constant split into three bf16 values (hi + mid + lo, exact
+//               to fp32 precision), so the softmax warps read no per-row data.
 //   warp 12     issues dV += P^T dO and dK += dS^T Q (A operand read from
 //               TMEM), then dQ^T = K^T dS^T into the dP^T columns (their
 //               dS^T has been consumed by dK).  Two issuing threads keep the
 //               tensor core fed while either one waits on a barrier.
 //   warps 0-7   two warpgroups, one thread per key row, each on 32 of the
-//               step's 64 query columns: P^T = exp2(S^T c - LSE log2 e),
-//               dS^T = P^T (dP^T - D) (packed f32x2 arithmetic), written as
+//               step's 64 query columns: P^T = exp2(S^T c), dS^T = P^T dP^T
+//               (shifted products, packed f32x2 arithmetic), written as
 //               bf16 over S^T / dP^T and dS^T also into a double-buffered
 //               swizzled SMEM tile; at the end of a unit the first warpgroup
 //               stores dK (scaled), the second dV.
@@ -71,9 +75,14 @@ struct Cfg {
     static constexpr int kQ0 = kV + kVTile;
     static constexpr int kDO0 = kQ0 + kQStages * kQTile;
     static constexpr int kDs0 = kDO0 + kQStages * kQTile;  // 2 buffers
-    static constexpr int kLse0 = kDs0 + 2 * kDsBytes;      // kQStages x BQ floats
-    static constexpr int kDel0 = kLse0 + kQStages * BQ * 4;
-    static constexpr int kBar = kDel0 + kQStages * BQ * 4;
+    // K = 16 slices that add -LSE/scale to S^T and -D to dP^T: a 128-row
+    // ones tile (the key side) and per stage one 64-row record tile for each
+    // (the query side), rows of 32 bytes, 32-byte swizzle
+    static constexpr int kAugTile = BQ * 32;
+    static constexpr int kOnes = kDs0 + 2 * kDsBytes;
+    static constexpr int kQA0 = kOnes + 128 * 32;
+    static constexpr int kDA0 = kQA0 + kQStages * kAugTile;
+    static constexpr int kBar = kDA0 + kQStages * kAugTile;
     // SFULL: S^T, dP^T of a step computed; PREADY: its P^T written to TMEM;
     // DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its dQ^T computed,
     // hence also its dV and dK (issued before it by the same thread), which
@@ -143,7 +152,8 @@ struct Shared {
 template <int D>
 __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, const WaitCtx& w,
                                          const CUtensorMap* tmq, const CUtensorMap* tmk,
-                                         const CUtensorMap* tmv, const CUtensorMap* tmdo)
+                                         const CUtensorMap* tmv, const CUtensorMap* tmdo,
+                                         const CUtensorMap* tmal, const CUtensorMap* tmad)
 {
     using C = Cfg<D>;
     const int lane = threadIdx.x & 31;
@@ -154,6 +164,8 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
         prefetch_tmap(tmk);
         prefetch_tmap(tmv);
         prefetch_tmap(tmdo);
+        prefetch_tmap(tmal);
+        prefetch_tmap(tmad);
     }
     uint32_t uc = 0, qc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -193,25 +205,17 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
                     __syncwarp();
                     if (*sh.abort_flag)
                         return;
-                    // LSE and D of the step's rows, copied asynchronously so that
-                    // the producer never waits on them; rows past the chunk read
-                    // as 0 (their P is masked).  Completion joins the Q/dO
-                    // barrier, whose phase cannot end before lane 0 arrives.
                     const int32_t m0 = i * BQ;
-                    const size_t rbase = (size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q + m0;
-                    const uint32_t sl = smem_u32(smem + C::kLse0 + st * BQ * 4);
-                    const uint32_t sd = smem_u32(smem + C::kDel0 + st * BQ * 4);
-#pragma unroll
-                    for (int c = lane; c < BQ; c += 32) {
-                        const bool in = m0 + c < p.chunk_q;
-                        cp_async_4(sl + 4 * c, in ? p.lse + rbase + c : p.lse, in ? 4u : 0u);
-                        cp_async_4(sd + 4 * c, in ? p.delta + rbase + c : p.delta, in ? 4u : 0u);
-                    }
-                    cp_async_mbar_arrive(&bar[C::QFULL + st]);
-                    __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&bar[C::QFULL + st], 2 * C::kQTile);
+                        mbar_arrive_expect_tx(&bar[C::QFULL + st],
+                                              2 * C::kQTile + 2 * C::kAugTile);
                         const int qrow = qr.p * p.chunk_q + m0;
+                        // the rows' -LSE/scale and -D records (rows past the
+                        // chunk read as zeros; their P is masked)
+                        tma_load_3d(smem + C::kQA0 + st * C::kAugTile, tmal, &bar[C::QFULL + st],
+                                    0, qrow, slice_q);
+                        tma_load_3d(smem + C::kDA0 + st * C::kAugTile, tmad, &bar[C::QFULL + st],
+                                    0, qrow, slice_q);
 #pragma unroll
                         for (int hb = 0; hb < D / 64; ++hb) {
                             tma_load_3d(smem + C::kQ0 + st * C::kQTile + hb * (BQ * 128), tmq,
@@ -256,6 +260,9 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
     const uint64_t dVk = sdesc_sw128(smem_u32(sh.smem + C::kV), 16, 1024);
     const uint64_t dQk = sdesc_sw128(smem_u32(sh.smem + C::kQ0), 16, 1024);
     const uint64_t dDOk = sdesc_sw128(smem_u32(sh.smem + C::kDO0), 16, 1024);
+    const uint64_t dOnes = sdesc_sw32(smem_u32(sh.smem + C::kOnes), 256);
+    const uint64_t dQA = sdesc_sw32(smem_u32(sh.smem + C::kQA0), 256);
+    const uint64_t dDA = sdesc_sw32(smem_u32(sh.smem + C::kDA0), 256);
     uint32_t uc = 0, m = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
@@ -278,6 +285,9 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
                 mma_ss(tmem + C::cS(b), sdesc_add(dKk, (kk >> 2) * 16384 + (kk & 3) * 32),
                        sdesc_add(dQk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
                        kk > 0);
+            // S^T - LSE/scale: one more K = 16 slice, ones against the records
+            mma_ss(tmem + C::cS(b), dOnes, sdesc_add(dQA, (m % C::kQStages) * C::kAugTile), idSt,
+                   1u);
             if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + b], ((m - 2) >> 1) & 1, w, 65))
                 return;
             tc_fence_after();
@@ -286,6 +296,9 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
                 mma_ss(tmem + C::cDP(b), sdesc_add(dVk, (kk >> 2) * 16384 + (kk & 3) * 32),
                        sdesc_add(dDOk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
                        kk > 0);
+            // dP^T - D, likewise
+            mma_ss(tmem + C::cDP(b), dOnes, sdesc_add(dDA, (m % C::kQStages) * C::kAugTile), idSt,
+                   1u);
             tc_commit(&bar[C::SFULL + b]);
         }
     }
@@ -365,8 +378,6 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     const int r = (warp & 3) * 32 + lane;    // key row inside the unit tile (TMEM lane)
     const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
-    const uint64_t nlog2e = f2pack(-1.4426950408889634f, -1.4426950408889634f);
-    const uint64_t neg1 = f2pack(-1.f, -1.f);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
@@ -393,8 +404,6 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         uint32_t sr[32], dr[32];
                         tmem_ld32(tl + C::cS(b) + 32 * h, sr);
                         tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
-                        const float* sl = (const float*)(sh.smem + C::kLse0 + st * BQ * 4) + 32 * h;
-                        const float* sd = (const float*)(sh.smem + C::kDel0 + st * BQ * 4) + 32 * h;
                         const bool full = (i >= qr.ifull) && ((i + 1) * BQ <= p.chunk_q) &&
                                           un.nvalid == kKvRows;
                         const int qbase = i * BQ + 32 * h;
@@ -406,14 +415,14 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         uint32_t pp[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            // two query columns 2j, 2j+1 at a time (f32x2):
-                            // P = exp2(S c - LSE log2 e).  A row without keys
-                            // (LSE = -inf) is never visible, so its P is masked.
-                            const uint64_t lp = *(const uint64_t*)(sl + 2 * j);
+                            // two query columns 2j, 2j+1 at a time (f32x2): the
+                            // tensor core already subtracted LSE/scale, so
+                            // P = exp2((S - LSE/scale) scale log2 e).  A row without
+                            // keys is never visible, so its P is masked.
                             float a0, a1;
-                            f2unpack(f2fma(f2pack(__uint_as_float(sr[2 * j]),
+                            f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]),
                                                   __uint_as_float(sr[2 * j + 1])),
-                                           c2x2, f2mul(lp, nlog2e)),
+                                           c2x2),
                                      a0, a1);
                             float p0 = ex2(a0), p1 = ex2(a1);
                             if (!full) {
@@ -431,17 +440,15 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         tmem_st_wait();
                         tc_fence_before();
                         mbar_arrive(&bar[C::PREADY + b]);
-                        // phase 2: dS^T = P^T (dP^T - D)
+                        // phase 2: dS^T = P^T (dP^T - D), D already subtracted
                         uint32_t dd[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const uint64_t dp = *(const uint64_t*)(sd + 2 * j);
                             float d0, d1;
                             f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]),
                                                   __uint_as_float(sr[2 * j + 1])),
-                                           f2fma(dp, neg1,
-                                                 f2pack(__uint_as_float(dr[2 * j]),
-                                                        __uint_as_float(dr[2 * j + 1])))),
+                                           f2pack(__uint_as_float(dr[2 * j]),
+                                                  __uint_as_float(dr[2 * j + 1]))),
                                      d0, d1);
                             dd[j] = pack_bf16x2(d0, d1);
                         }
@@ -579,7 +586,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
-                    const __grid_constant__ BwdParams p)
+                    const __grid_constant__ CUtensorMap tmal,
+                    const __grid_constant__ CUtensorMap tmad, const __grid_constant__ BwdParams p)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -609,6 +617,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar[C::DKVFULL], 1);
         fence_barrier_init();
     }
+    {
+        // the ones tile: every 32-byte row holds 1.0 at K positions 0, 1, 8
+        // and 9; its two 16-byte halves are equal, so the swizzle leaves it
+        // as is
+        uint4* ones = (uint4*)(smem + C::kOnes);
+        for (int i = threadIdx.x; i < 128 * 2; i += blockDim.x)
+            ones[i] = make_uint4(0x3F803F80u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     if (D < 128) {
         // zero the K tile's padding columns once (TMA never writes them)
         uint4* pad = (uint4*)(smem + C::kK + 16384);
@@ -628,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 12) {
         reg_dealloc<kRegsCtl>();
         if (warp == kWarpProducer) {
-            producer<D>(p, sh, wctx, &tmq, &tmk, &tmv, &tmdo);
+            producer<D>(p, sh, wctx, &tmq, &tmk, &tmv, &tmdo, &tmal, &tmad);
             if (lane == 0 && *abort_flag) {
                 // give copies already issued a bounded chance to land
                 const uint64_t t0 = globaltimer_ns();
@@ -660,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace bwd
 
 cudaError_t launch_attn_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tal, const CUtensorMap& tad, const BwdParams& p,
                             int grid, cudaStream_t stream)
 {
     if (d == 128) {
@@ -669,14 +687,14 @@ cudaError_t launch_attn_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+        bwd::attn_bwd_kernel<128><<<grid, bwd::kThreads, smem, stream>>>(tq, tk, tv, tdo, tal, tad, p);
     } else {
         constexpr int smem = bwd::Cfg<64>::kSmem;
         cudaError_t e = cudaFuncSetAttribute(bwd::attn_bwd_kernel<64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+        bwd::attn_bwd_kernel<64><<<grid, bwd::kThreads, smem, stream>>>(tq, tk, tv, tdo, tal, tad, p);
     }
     return cudaGetLastError();
 }

@@ -193,12 +193,30 @@ cudaError_t launch_permute(const PermuteParams& pp, const void* in, void* out, i
 // and dq_acc[r][:] = 0 when dq_acc is non-null.  D/8 threads per row, 16
 // bytes of each bf16 tensor per thread.
 // ---------------------------------------------------------------------------
+// One K = 16 slice record that adds x to a product through the tensor core:
+// x split into three bf16 values hi + mid + lo (|x - hi - mid - lo| <= 2^-24
+// |x|, the precision of fp32) at K positions 0, 1 and 8, zeros elsewhere;
+// the matching operand row holds ones at K positions 0, 1, 8 and 9.
+__device__ __forceinline__ void aug_record(float x, uint4* dst)
+{
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    dst[0] = make_uint4((uint32_t)__bfloat16_as_ushort(hi) |
+                            ((uint32_t)__bfloat16_as_ushort(mid) << 16),
+                        0u, 0u, 0u);
+    dst[1] = make_uint4((uint32_t)__bfloat16_as_ushort(lo), 0u, 0u, 0u);
+}
+
+// Per row: D = dO . O (or the caller's delta), the records of -LSE/scale
+// (0 for a row without keys, whose P is masked anyway) and -D, and zeroing
+// of the fp32 dQ accumulator row.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows,
-                                                             const uint4* __restrict__ o,
-                                                             const uint4* __restrict__ dout,
-                                                             float* __restrict__ delta,
-                                                             float4* __restrict__ dq_acc)
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(
+    int64_t rows, const uint4* __restrict__ o, const uint4* __restrict__ dout,
+    const float* __restrict__ delta, const float* __restrict__ lse, float inv_scale,
+    uint4* __restrict__ aug_lse, uint4* __restrict__ aug_delta, float4* __restrict__ dq_acc)
 {
     constexpr int TPR = D / 8;
     constexpr int RPB = 256 / TPR;
@@ -207,20 +225,28 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows,
     for (int64_t rb = (int64_t)blockIdx.x * RPB; rb < rows; rb += (int64_t)gridDim.x * RPB) {
         const int64_t r = rb + threadIdx.x / TPR;
         const bool ok = r < rows;
-        const uint4 a = ok ? __ldg(o + r * TPR + sub) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 b = ok ? __ldg(dout + r * TPR + sub) : make_uint4(0u, 0u, 0u, 0u);
-        float s = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x);
-        s = fmaf(bf16lo(a.y), bf16lo(b.y), s);
-        s = fmaf(bf16hi(a.y), bf16hi(b.y), s);
-        s = fmaf(bf16lo(a.z), bf16lo(b.z), s);
-        s = fmaf(bf16hi(a.z), bf16hi(b.z), s);
-        s = fmaf(bf16lo(a.w), bf16lo(b.w), s);
-        s = fmaf(bf16hi(a.w), bf16hi(b.w), s);
+        float s = 0.f;
+        if (o) {
+            const uint4 a = ok ? __ldg(o + r * TPR + sub) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 b = ok ? __ldg(dout + r * TPR + sub) : make_uint4(0u, 0u, 0u, 0u);
+            s = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x);
+            s = fmaf(bf16lo(a.y), bf16lo(b.y), s);
+            s = fmaf(bf16hi(a.y), bf16hi(b.y), s);
+            s = fmaf(bf16lo(a.z), bf16lo(b.z), s);
+            s = fmaf(bf16hi(a.z), bf16hi(b.z), s);
+            s = fmaf(bf16lo(a.w), bf16lo(b.w), s);
+            s = fmaf(bf16hi(a.w), bf16hi(b.w), s);
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1)
-            s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (ok && sub == 0)
-            delta[r] = s;
+            for (int off = TPR / 2; off > 0; off >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, off);
+        } else if (ok && sub == 0) {
+            s = delta[r];
+        }
+        if (ok && sub == 0) {
+            const float l = lse[r];
+            aug_record(l == -INFINITY ? 0.f : -l * inv_scale, aug_lse + 2 * r);
+            aug_record(-s, aug_delta + 2 * r);
+        }
         if (ok && dq_acc) {
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
             dq_acc[r * (D / 4) + 2 * sub] = z;
@@ -230,7 +256,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(int64_t rows,
 }
 
 cudaError_t launch_bwd_preprocess(int64_t rows, int d, const void* o, const void* dout,
-                                  float* delta, float* dq_acc, int num_sms, cudaStream_t stream)
+                                  const float* delta, const float* lse, float scale,
+                                  void* aug_lse, void* aug_delta, float* dq_acc, int num_sms,
+                                  cudaStream_t stream)
 {
     const int rpb = 256 / (d / 8);
     int64_t blocks = (rows + rpb - 1) / rpb;
@@ -239,12 +267,15 @@ cudaError_t launch_bwd_preprocess(int64_t rows, int d, const void* o, const void
         blocks = cap;
     if (blocks < 1)
         blocks = 1;
+    const float inv = 1.f / scale;
     if (d == 128)
         bwd_preprocess_kernel<128><<<(int)blocks, 256, 0, stream>>>(
-            rows, (const uint4*)o, (const uint4*)dout, delta, (float4*)dq_acc);
+            rows, (const uint4*)o, (const uint4*)dout, delta, lse, inv, (uint4*)aug_lse,
+            (uint4*)aug_delta, (float4*)dq_acc);
     else
         bwd_preprocess_kernel<64><<<(int)blocks, 256, 0, stream>>>(
-            rows, (const uint4*)o, (const uint4*)dout, delta, (float4*)dq_acc);
+            rows, (const uint4*)o, (const uint4*)dout, delta, lse, inv, (uint4*)aug_lse,
+            (uint4*)aug_delta, (float4*)dq_acc);
     return cudaGetLastError();
 }
 

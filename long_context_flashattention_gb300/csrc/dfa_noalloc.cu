@@ -52,15 +52,16 @@ extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void
 {
     if (!desc)
         return dfa::set_error(DFA_ERR_INVALID_ARG, "desc is NULL");
-    // scratch this problem needs: status word + fp32 dQ accumulator + D
+    // scratch this problem needs: status word + fp32 dQ accumulator + the
+    // 32-byte -LSE/scale and -D records of every query row
     const size_t rows = (size_t)(desc->B > 0 ? desc->B : 0) * (size_t)(desc->Hq > 0 ? desc->Hq : 0) *
                         (size_t)(desc->N > 0 ? desc->N : 0);
     const size_t need = kStatusBytes + align256(rows * (size_t)(desc->d > 0 ? desc->d : 0) * 4) +
-                        align256(rows * 4);
+                        2 * align256(rows * 32);
     if (need > kNoAllocScratchBytes)
         return dfa::set_error(DFA_ERR_WORKSPACE,
                               "dfa_attn_bwd_noalloc: this problem needs %zu bytes of scratch "
-                              "(256 + B*Hq*N*(4d + 4), rounded), above the fixed %zu",
+                              "(256 + B*Hq*N*(4d + 64), rounded), above the fixed %zu",
                               need, kNoAllocScratchBytes);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -78,8 +79,8 @@ extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void
         }
         scratch = g_scratch_ptr[dev];
     }
-    // The status word must start at zero; the dQ accumulator and D are
-    // rewritten by the backward's own preprocess step.
+    // The status word must start at zero; the dQ accumulator and the records
+    // are rewritten by the backward's own preprocess step.
     const cudaError_t e = cudaMemsetAsync(scratch, 0, kStatusBytes, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: %s", cudaGetErrorString(e));

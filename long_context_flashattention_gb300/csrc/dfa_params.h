@@ -167,8 +167,6 @@ struct BwdParams {
     UnitTable units;
     DevMap qmap[kMaxChunks];
     DevMap kmap[kMaxChunks];
-    const float* lse;            // [BHq, Lq]
-    const float* delta;          // [BHq, Lq]
     float* dq_acc;               // [BHq, Lq, d] fp32, scaled
     void* dk;                    // [BHkv, Lk, d]
     void* dv;

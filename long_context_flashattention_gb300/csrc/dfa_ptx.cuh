@@ -274,6 +274,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// Shared-memory matrix descriptor, 32-byte swizzle, K-major rows of exactly
+// 32 bytes (one K = 16 slice of bf16): 8-row groups are sbo_bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;  // leading byte offset: unused for this layout
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)6 << 61;
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // TMEM <-> registers.  32x32b shape: warp w reaches lanes [32 (w%4), +32);
 // thread t of the warp gets lane 32 (w%4) + t, columns [col, col + n).
