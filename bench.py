@@ -279,6 +279,60 @@ def run_gpu(args):
     merge_bytes = rows * (P * (4 * w.d + 4) + (2 * w.d + 4))
     del parts_o, parts_l
 
+    # permute fused with the rotary embedding at global positions, on Q
+    r_out = torch.empty_like(qg)
+    for _ in range(3):
+        dfa.permute_rope(qg, P, kind, out=r_out)
+    torch.cuda.synchronize(dev)
+    m0.record(stream)
+    for _ in range(reps):
+        dfa.permute_rope(qg, P, kind, out=r_out)
+    m1.record(stream)
+    torch.cuda.synchronize(dev)
+    rope_ms = m0.elapsed_time(m1) / reps
+    rope_bytes = 2 * qg.numel() * qg.element_size()
+    del r_out
+
+    # the ring schedule on one GPU (P workers, K/V hand-over on a second stream)
+    n = w.N // P
+    pq, pk, pv = bufs["perm"][:3]
+    qc, kc, vc = ([t[:, :, p * n:(p + 1) * n].contiguous() for p in range(P)]
+                  for t in (pq, pk, pv))
+    slots = [torch.empty(4 * kc[0].numel(), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    outs = dfa.ring_fwd(qc, kc, vc, kind, slots=slots)
+    ring_ws = dfa.new_workspace(dfa.make_desc(w.B, w.Hq, w.Hkv, w.N, w.d, P=P, partition=kind),
+                                dfa.OP_RING_FWD, dev)
+
+    def timed(fn, rep=2):
+        torch.cuda.synchronize(dev)
+        m0.record(stream)
+        for _ in range(rep):
+            fn()
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        return m0.elapsed_time(m1) / rep
+
+    ring_ov = timed(lambda: dfa.ring_fwd(qc, kc, vc, kind, slots=slots, outs=outs, ws=ring_ws))
+    ring_se = timed(lambda: dfa.ring_fwd(qc, kc, vc, kind, slots=slots, outs=outs, ws=ring_ws,
+                                         overlap=False))
+
+    def copies_alone():
+        for _ in range(P - 1):
+            for p in range(P):
+                slots[p][:kc[0].numel()].copy_(kc[(p - 1) % P].view(-1))
+                slots[p][kc[0].numel():2 * kc[0].numel()].copy_(vc[(p - 1) % P].view(-1))
+
+    ring_cp = timed(copies_alone)
+    del qc, kc, vc, slots, outs, ring_ws
+
+    # split-KV decoding: one new token per head against this workload's K/V as the cache
+    dq_in = qg[:, :, -1:].contiguous()
+    dec_out = dfa.decode(dq_in, kg, vg, split_len=1024)
+    dec_ms = timed(lambda: dfa.decode(dq_in, kg, vg, split_len=1024, out=dec_out[0],
+                                      lse=dec_out[1]), rep=10)
+    dec_bytes = 2 * kg.numel() * kg.element_size()
+    del dq_in, dec_out
+
     pk, src = peaks()
     flops = w.flops_fwd + w.flops_bwd
     value = flops * world / (step_ms * 1e-3) / 1e12
@@ -322,6 +376,21 @@ def run_gpu(args):
                   "bytes": merge_bytes, "ms": round(merge_ms, 4),
                   "achieved": round(merge_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                   "frac": round(merge_gbs / pk["hbm_gbs"], 4)},
+        "rope_permute": {"kernel": "dfa::permute_rope_kernel", "tensor": "Q",
+                         "bytes": rope_bytes, "ms": round(rope_ms, 4),
+                         "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
+        "ring_fwd": {"P": P, "partition": kind, "ms_overlap": round(ring_ov, 3),
+                     "ms_serial": round(ring_se, 3), "ms_copies_alone": round(ring_cp, 3),
+                     "tflops_overlap": round(w.flops_fwd / (ring_ov * 1e-3) / 1e12, 2),
+                     "copy_hidden_frac": round(max(0.0, ring_se - ring_ov) / ring_cp, 3)
+                     if ring_cp > 0 else None},
+        "decode": {"kernel": "dfa::dec::decode_split_kernel + lse_merge", "T": 1,
+                   "L": w.N, "split_len": 1024, "bytes": dec_bytes, "ms": round(dec_ms, 4),
+                   "achieved": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
+                   "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(dec_bytes / (dec_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

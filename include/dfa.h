@@ -111,7 +111,8 @@ typedef struct dfa_chunk_pair {
 } dfa_chunk_pair;
 
 /* Operations for dfa_workspace_size. */
-enum { DFA_OP_FWD = 0, DFA_OP_BWD = 1, DFA_OP_CHUNK_FWD = 2, DFA_OP_CHUNK_BWD = 3 };
+enum { DFA_OP_FWD = 0, DFA_OP_BWD = 1, DFA_OP_CHUNK_FWD = 2, DFA_OP_CHUNK_BWD = 3,
+       DFA_OP_RING_FWD = 4 };
 
 /*
  * dfa_attn_fwd -- attention forward over a whole sequence (FlashAttention
@@ -202,6 +203,61 @@ dfa_status dfa_lse_merge(int64_t rows, int32_t d, int32_t k, const float* o_part
                          int32_t out_fp32, int32_t accumulate, void* stream);
 
 /*
+ * dfa_ring_fwd -- the ring schedule of context-parallel attention on one GPU
+ * (DistFlashAttn Guide, the ring over P workers; Striped Attention Guide,
+ * "Workload Balance Theorem": at ring step s worker p holds the key/value
+ * chunk of worker (p - s) mod P, and "Incremental Online Softmax Rescaling":
+ * each step's partial is merged into the worker's running result).
+ * Worker p holds chunk p of desc's partition (P workers, chunks of n = N/P
+ * tokens, in worker-major order as dfa_permute produces them).  At each of
+ * the P steps every worker runs dfa_chunk_fwd against the K/V chunk it
+ * holds and merges the partial into its (o, lse) with dfa_lse_merge; the
+ * hand-over of K/V to the next worker is a device-to-device copy into one of
+ * the receiver's two slots, issued on copy_stream while the step computes
+ * (overlap = 1), or on compute_stream before it (overlap = 0, for timing the
+ * difference).  The result equals attention over the whole sequence.
+ *   workers[p].q [B,Hq,n,d], .k/.v [B,Hkv,n,d] bf16 (read only);
+ *   .kv_slots 4 * B*Hkv*n*d bf16 (the two receive slots, K then V each);
+ *   .o [B,Hq,n,d] fp32 and .lse [B,Hq,n] fp32 (written).
+ *   ws: dfa_workspace_size(desc, DFA_OP_RING_FWD) bytes (a partial's O, LSE).
+ * Both streams are the caller's; when the call returns all work is ordered
+ * before later work on compute_stream.
+ */
+typedef struct dfa_ring_worker {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* kv_slots;
+    float* o;
+    float* lse;
+} dfa_ring_worker;
+
+dfa_status dfa_ring_fwd(const dfa_attn_desc* desc, const dfa_ring_worker* workers, void* ws,
+                        size_t ws_bytes, int32_t overlap, void* compute_stream,
+                        void* copy_stream);
+
+/*
+ * dfa_decode -- split-KV decoding: T query tokens per sequence against L
+ * cached keys (FlashAttention glossary entry, the Flash-Decoding variant:
+ * the keys are cut into splits of split_len, each split gives a normalised
+ * partial (O, LSE) on its own CTAs, and the partials are merged by the LSE
+ * rescaling of dfa_lse_merge).  Query token t sits at position q_pos0 + t,
+ * cached key j at position j; with desc->causal, key j is visible to token t
+ * iff j <= q_pos0 + t.  desc supplies B, Hq, Hkv, d, causal, scale, o_fp32.
+ *   q [B,Hq,T,d] bf16; k, v [B,Hkv,L,d] bf16;
+ *   o [B,Hq,T,d] bf16 (o_fp32 = 0) or fp32; lse [B,Hq,T] fp32.
+ *   split_len: a positive multiple of 64; (Hq/Hkv) * T <= 16.
+ *   ws: dfa_decode_workspace_size(desc, T, L, split_len) bytes (partials).
+ * The split partials run on CUDA cores (every K/V row is read once and meets
+ * a handful of query rows: memory-bound, not a tensor-core contraction).
+ */
+size_t dfa_decode_workspace_size(const dfa_attn_desc* desc, int32_t T, int64_t L,
+                                 int32_t split_len);
+dfa_status dfa_decode(const dfa_attn_desc* desc, int32_t T, int64_t L, int64_t q_pos0,
+                      const void* q, const void* k, const void* v, void* o, float* lse,
+                      int32_t split_len, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dfa_permute -- gather rows between natural order and the worker-major order
  * of desc's partition (Striped Attention Guide, the partitioner's
  * stripe/unstripe; DistFlashAttn Guide, "The Folded Chunk Assignment").
@@ -211,6 +267,27 @@ dfa_status dfa_lse_merge(int64_t rows, int32_t d, int32_t k, const float* o_part
  */
 dfa_status dfa_permute(const dfa_attn_desc* desc, int32_t inverse, const void* in, void* out,
                        int32_t elem_bytes, int64_t row_elems, int64_t heads, void* stream);
+
+/*
+ * dfa_permute_rope -- dfa_permute of bf16 query or key rows fused with the
+ * rotary position embedding at each token's global position (Striped
+ * Attention Guide, "Preserving Rotary Position Embeddings": token i is
+ * rotated by R(Theta, i) using its absolute index, i = m P + p for a
+ * token-striped worker p, before the ring, so that rotated inner products
+ * depend only on i - j whatever the storage order).
+ * Rotation: feature pairs (2t, 2t+1), t < d/2, turned by the angle
+ * i * theta_base^(-2t/d) (x' = x cos - y sin, y' = x sin + y cos), computed
+ * in fp32 after an fp64 reduction of the angle, rounded to bf16.
+ *   in, out: [heads, N, d] bf16 (d = desc->d), 16-byte aligned, not
+ *   overlapping; heads = B * H.  inverse = 0: natural order in, worker-major
+ *   order out, rotation by +angle; inverse = 1: worker-major in, natural out,
+ *   rotation by -angle (the transpose, for gradients dQ and dK).
+ *   theta_base: > 1 (10000 for Llama-7B).
+ * Returns DFA_ERR_INVALID_ARG on a bad descriptor, NULL or overlapping
+ * buffers or a bad base, DFA_ERR_UNSUPPORTED on misaligned pointers.
+ */
+dfa_status dfa_permute_rope(const dfa_attn_desc* desc, int32_t inverse, const void* in,
+                            void* out, int64_t heads, float theta_base, void* stream);
 
 /*
  * Ring schedule (host only, no device work).  For the P workers of desc's

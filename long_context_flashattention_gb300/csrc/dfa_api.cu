@@ -494,7 +494,7 @@ int32_t dfa_version(void) { return 1; }
 
 size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op)
 {
-    if (check_desc(desc, op == DFA_OP_FWD || op == DFA_OP_BWD) != DFA_OK)
+    if (check_desc(desc, op == DFA_OP_FWD || op == DFA_OP_BWD || op == DFA_OP_RING_FWD) != DFA_OK)
         return 0;
     switch (op) {
     case DFA_OP_FWD:
@@ -502,6 +502,10 @@ size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op)
         return kStatusBytes;
     case DFA_OP_BWD:
         return bwd_ws_bytes(*desc);
+    case DFA_OP_RING_FWD: {
+        const size_t rows = (size_t)desc->B * desc->Hq * (size_t)(desc->N / desc->P);
+        return kStatusBytes + align256(rows * desc->d * 4) + align256(rows * 4);
+    }
     case DFA_OP_CHUNK_BWD:
         return kStatusBytes +
                2 * align256((size_t)desc->B * desc->Hq * (size_t)desc->N * kAugRowBytes);
@@ -701,6 +705,113 @@ dfa_status dfa_permute(const dfa_attn_desc* desc, int32_t inverse, const void* i
     cudaError_t e = launch_permute(pp, in, out, vb, num_sms(), (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "permute launch");
+    return DFA_OK;
+}
+
+dfa_status dfa_permute_rope(const dfa_attn_desc* desc, int32_t inverse, const void* in,
+                            void* out, int64_t heads, float theta_base, void* stream)
+{
+    dfa_status s = check_desc(desc, true);
+    if (s != DFA_OK)
+        return s;
+    if (!in || !out)
+        return fail(DFA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(in) || !aligned16(out))
+        return fail(DFA_ERR_UNSUPPORTED, "tensor pointers must be 16-byte aligned");
+    if (heads < 1 || heads > (1 << 24))
+        return fail(DFA_ERR_INVALID_ARG, "heads must be in [1, 2^24]");
+    if (!(theta_base > 1.f) || !std::isfinite(theta_base))
+        return fail(DFA_ERR_INVALID_ARG, "theta_base must be finite and > 1");
+    const int64_t bytes = heads * desc->N * (int64_t)desc->d * 2;
+    const char* a = (const char*)in;
+    const char* b = (const char*)out;
+    if (a < b + bytes && b < a + bytes)
+        return fail(DFA_ERR_INVALID_ARG, "in and out overlap");
+    RopeParams rp;
+    memset(&rp, 0, sizeof rp);
+    PermuteParams& pp = rp.perm;
+    pp.heads = heads;
+    pp.N = (int32_t)desc->N;
+    pp.P = desc->P;
+    pp.n = (int32_t)(desc->N / desc->P);
+    pp.inverse = inverse ? 1 : 0;
+    pp.row_vecs = desc->d / 8;
+    for (int p = 0; p < desc->P; ++p)
+        pp.map[p] = to_dev(partition_map(*desc, p));
+    rp.d = desc->d;
+    for (int t = 0; t < desc->d / 2; ++t)
+        rp.theta[t] = std::pow((double)theta_base, -2.0 * t / desc->d);
+    cudaError_t e = launch_permute_rope(rp, in, out, num_sms(), (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "permute with rotary embedding launch");
+    return DFA_OK;
+}
+
+size_t dfa_decode_workspace_size(const dfa_attn_desc* desc, int32_t T, int64_t L,
+                                 int32_t split_len)
+{
+    if (check_desc(desc, false) != DFA_OK || T < 1 || L < 1 || split_len < 64 ||
+        split_len % 64 != 0)
+        return 0;
+    const size_t splits = (size_t)((L + split_len - 1) / split_len);
+    const size_t rows = (size_t)desc->B * desc->Hq * (size_t)T;
+    return kStatusBytes + align256(splits * rows * desc->d * 4) + align256(splits * rows * 4);
+}
+
+dfa_status dfa_decode(const dfa_attn_desc* desc, int32_t T, int64_t L, int64_t q_pos0,
+                      const void* q, const void* k, const void* v, void* o, float* lse,
+                      int32_t split_len, void* ws, size_t ws_bytes, void* stream)
+{
+    dfa_status s = check_desc(desc, false);
+    if (s != DFA_OK)
+        return s;
+    if (T < 1 || L < 1 || L >= INT32_MAX || q_pos0 < 0)
+        return fail(DFA_ERR_INVALID_ARG, "need T >= 1, 1 <= L < 2^31, q_pos0 >= 0");
+    if (split_len < 64 || split_len % 64 != 0)
+        return fail(DFA_ERR_INVALID_ARG, "split_len must be a positive multiple of 64");
+    const int G = desc->Hq / desc->Hkv;
+    if ((int64_t)G * T > decode_max_rows())
+        return fail(DFA_ERR_UNSUPPORTED, "decode handles at most %d query rows per key/value "
+                    "head (Hq/Hkv * T)", decode_max_rows());
+    if ((s = check_ptrs({q, k, v, o})) != DFA_OK)
+        return s;
+    if (!lse)
+        return fail(DFA_ERR_INVALID_ARG, "lse is NULL");
+    const size_t need = dfa_decode_workspace_size(desc, T, L, split_len);
+    if ((s = check_ws(ws, ws_bytes, need)) != DFA_OK)
+        return s;
+    const int splits = (int)((L + split_len - 1) / split_len);
+    if ((int64_t)splits > 65535 * 1024)
+        return fail(DFA_ERR_UNSUPPORTED, "too many splits");
+    const size_t rows = (size_t)desc->B * desc->Hq * (size_t)T;
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.B = desc->B;
+    p.Hq = desc->Hq;
+    p.Hkv = desc->Hkv;
+    p.G = G;
+    p.T = T;
+    p.L = (int32_t)L;
+    p.split_len = split_len;
+    p.causal = desc->causal;
+    p.q_pos0 = q_pos0;
+    p.scale_log2 = desc->scale * 1.4426950408889634f;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o_part = reinterpret_cast<float*>((char*)ws + kStatusBytes);
+    p.lse_part = reinterpret_cast<float*>((char*)ws + kStatusBytes +
+                                          align256((size_t)splits * rows * desc->d * 4));
+    cudaStream_t st = (cudaStream_t)stream;
+    if ((int64_t)desc->B * desc->Hkv > 65535)
+        return fail(DFA_ERR_UNSUPPORTED, "B * Hkv must be at most 65535");
+    cudaError_t e = launch_decode_split(desc->d, p, splits, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode launch");
+    e = launch_lse_merge((int64_t)rows, desc->d, splits, p.o_part, p.lse_part, o, lse,
+                         desc->o_fp32, 0, num_sms(), st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "merge launch");
     return DFA_OK;
 }
 

@@ -29,6 +29,11 @@ cudaError_t launch_lse_merge(int64_t rows, int d, int k, const float* o_parts,
                              int accumulate, int num_sms, cudaStream_t stream);
 cudaError_t launch_permute(const PermuteParams& pp, const void* in, void* out, int vec_bytes,
                            int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_split(int d, const DecodeParams& p, int splits, cudaStream_t stream);
+int decode_max_rows();
+struct RopeParams;
+cudaError_t launch_permute_rope(const RopeParams& rp, const void* in, void* out, int num_sms,
+                                cudaStream_t stream);
 // Per query row of the backward: the 32-byte K-slice records of -LSE/scale
 // and -D (D = dO . O computed here from o and dout, or read from delta when
 // o is NULL), and, if dq_acc is not NULL, zeroing of its dQ accumulator row.

@@ -1,6 +1,7 @@
 // dfa_mem.cu -- the bandwidth-bound kernels: log-sum-exp merge of partial
-// results, sequence permutes between natural and worker-major order, the
-// backward preprocess (D = rowsum(dO * O), zeroing the dQ accumulator), the
+// results, sequence permutes between natural and worker-major order (plain, or
+// with the rotary embedding at global positions), the backward preprocess
+// (D = rowsum(dO * O), the row-constant records, zeroing the dQ accumulator), the
 // dQ fp32 -> bf16 conversion, and the bounded-wait self-test.
 //
 // All are grid-stride loops over 16-byte vectors with several independent
@@ -189,9 +190,77 @@ cudaError_t launch_permute(const PermuteParams& pp, const void* in, void* out, i
 }
 
 // ---------------------------------------------------------------------------
-// Backward preprocess: delta[r] = sum_c dO[r][c] * O[r][c] (fp32 accumulate),
-// and dq_acc[r][:] = 0 when dq_acc is non-null.  D/8 threads per row, 16
-// bytes of each bf16 tensor per thread.
+// Permute with rotary position embedding at the tokens' global positions
+// (Striped Attention Guide, "Preserving Rotary Position Embeddings": the
+// rotation R(Theta, i) of token i is applied with its absolute position i,
+// i = m P + p for token-striped storage, before the ring).  Feature pairs
+// (2t, 2t+1) are rotated by the angle i * theta_t; `inverse` applies the
+// transposed rotation and the inverse permutation (the gradient path).
+// ---------------------------------------------------------------------------
+// One warp per token row at a time: lane l owns 16-byte vector v = l mod V
+// (V = d/8 vectors per head row, 4 feature pairs each) of heads l div V,
+// l div V + 32/V, ...; it reduces its own 4 angles (in fp64: i * theta_t
+// reaches 5e5 radians at N = 512K, where an fp32 product would be off by up
+// to 0.03), so no shared memory or block barrier is needed.
+__global__ void __launch_bounds__(256) permute_rope_kernel(const __grid_constant__ RopeParams rp,
+                                                           const uint4* __restrict__ in,
+                                                           uint4* __restrict__ out)
+{
+    const PermuteParams& p = rp.perm;
+    const int vecs = rp.d / 8;             // 8 or 16
+    const int lane = threadIdx.x & 31;
+    const int v = lane & (vecs - 1);
+    const int h0 = lane / vecs, hstep = 32 / vecs;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    constexpr double kTwoPi = 6.283185307179586;
+    for (int32_t r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < p.N; r += warps) {
+        const int32_t w = r / p.n, m = r - w * p.n;
+        const int32_t g = map_pos(p.map[w], m);  // natural row = global position
+        float2 cs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            // Cody-Waite style reduction of the angle into [-pi, pi] in fp64
+            const double a = (double)g * rp.theta[4 * v + e];
+            const double k = rint(a * (1.0 / kTwoPi));
+            const float red = (float)fma(-k, kTwoPi, a);
+            float sn, c;
+            sincosf(red, &sn, &c);
+            cs[e] = make_float2(c, p.inverse ? -sn : sn);
+        }
+#pragma unroll 4
+        for (int64_t h = h0; h < p.heads; h += hstep) {
+            const int64_t wm = (h * p.N + r) * vecs + v;
+            const int64_t nat = (h * p.N + g) * vecs + v;
+            const uint4 x = __ldg(in + (p.inverse ? wm : nat));
+            uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = bf16lo(xs[e]), b = bf16hi(xs[e]);
+                xs[e] = pack_bf16x2(a * cs[e].x - b * cs[e].y, a * cs[e].y + b * cs[e].x);
+            }
+            out[p.inverse ? nat : wm] = make_uint4(xs[0], xs[1], xs[2], xs[3]);
+        }
+    }
+}
+
+cudaError_t launch_permute_rope(const RopeParams& rp, const void* in, void* out, int num_sms,
+                                cudaStream_t stream)
+{
+    int64_t blocks = (rp.perm.N + 7) / 8;  // 8 warps per block, a row each
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    permute_rope_kernel<<<(int)blocks, 256, 0, stream>>>(rp, (const uint4*)in, (uint4*)out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Backward preprocess: D[r] = sum_c dO[r][c] * O[r][c] (fp32 accumulate) or
+// the caller's D, the per-row records of -LSE/scale and -D for the tensor
+// core, and dq_acc[r][:] = 0 when dq_acc is non-null.  D/8 threads per row,
+// 16 bytes of each bf16 tensor per thread.
 // ---------------------------------------------------------------------------
 // One K = 16 slice record that adds x to a product through the tensor core:
 // x split into three bf16 values hi + mid + lo (|x - hi - mid - lo| <= 2^-24

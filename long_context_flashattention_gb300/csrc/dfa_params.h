@@ -133,6 +133,29 @@ struct PermuteParams {
     DevMap map[kMaxChunks];
 };
 
+// Split-KV decoding: T query tokens per sequence against L cached keys.
+struct DecodeParams {
+    int32_t B, Hq, Hkv, G, T;
+    int32_t L;                   // cached keys per (b, kv head)
+    int32_t split_len;           // keys per split (multiple of 64)
+    int32_t causal;
+    int64_t q_pos0;              // position of query token 0; key j is at position j
+    float scale_log2;            // scale * log2(e)
+    const void* q;               // [B, Hq, T, d] bf16
+    const void* k;               // [B, Hkv, L, d] bf16
+    const void* v;
+    float* o_part;               // [splits, B*Hq*T, d] fp32
+    float* lse_part;             // [splits, B*Hq*T] fp32
+};
+
+// Rotary embedding fused into the permute: theta[t] = base^(-2t/d) for the
+// feature pairs (2t, 2t+1), t < d/2.
+struct RopeParams {
+    PermuteParams perm;
+    int32_t d;
+    double theta[64];
+};
+
 // Forward kernel parameters.
 struct FwdParams {
     int32_t BH, Hq, Hkv, G;

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libdfa.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "dfa.h")
 
 PARTITIONS = {"contiguous": 0, "balanced": 1, "striped": 2}
-OP_FWD, OP_BWD, OP_CHUNK_FWD, OP_CHUNK_BWD = 0, 1, 2, 3
+OP_FWD, OP_BWD, OP_CHUNK_FWD, OP_CHUNK_BWD, OP_RING_FWD = 0, 1, 2, 3, 4
 STATUS = {0: "DFA_OK", 1: "DFA_ERR_INVALID_ARG", 2: "DFA_ERR_UNSUPPORTED",
           3: "DFA_ERR_WORKSPACE", 4: "DFA_ERR_CUDA", 5: "DFA_ERR_TIMEOUT"}
 
@@ -45,6 +45,11 @@ class PosMap(ctypes.Structure):
 
 class ChunkPair(ctypes.Structure):
     _fields_ = [("q", PosMap), ("kv", PosMap)]
+
+
+class RingWorker(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("kv_slots", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
 class Schedule(ctypes.Structure):
@@ -79,6 +84,10 @@ def lib():
                                     vp, vp, vp, vp, vp, vp, sz, vp]),
             "dfa_lse_merge": (i32, [i64, i32, i32, vp, vp, vp, vp, i32, i32, vp]),
             "dfa_permute": (i32, [D, i32, vp, vp, i32, i64, i64, vp]),
+            "dfa_permute_rope": (i32, [D, i32, vp, vp, i64, ctypes.c_float, vp]),
+            "dfa_ring_fwd": (i32, [D, ctypes.POINTER(RingWorker), vp, sz, i32, vp, vp]),
+            "dfa_decode_workspace_size": (sz, [D, i32, i64, i32]),
+            "dfa_decode": (i32, [D, i32, i64, i64, vp, vp, vp, vp, vp, i32, vp, sz, vp]),
             "dfa_make_schedule": (i32, [D, i32, i32, ctypes.POINTER(Schedule)]),
             "dfa_partition_map": (i32, [D, i32, ctypes.POINTER(PosMap)]),
             "dfa_workspace_size": (sz, [D, i32]),
@@ -292,6 +301,83 @@ def permute(x, P, partition, inverse=False, stripe=1, out=None, stream=None):
     _check(lib().dfa_permute(ctypes.byref(desc), int(inverse), _ptr(x), _ptr(out),
                              x.element_size(), row, B * H, _stream(stream)))
     return out
+
+
+def permute_rope(x, P, partition, inverse=False, stripe=1, theta_base=10000.0, out=None,
+                 stream=None):
+    """dfa_permute of bf16 [B,H,N,d] query or key rows with the rotary embedding
+    applied at each token's global position (inverse: the transposed rotation
+    and the inverse permutation, for dQ / dK)."""
+    _need_cuda(x)
+    if x.dim() != 4 or x.dtype != torch.bfloat16:
+        raise ValueError("expected bf16 [B,H,N,d]")
+    B, H, N, d = x.shape
+    desc = make_desc(1, 1, 1, N, d, P=P, partition=partition, stripe=stripe)
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().dfa_permute_rope(ctypes.byref(desc), int(inverse), _ptr(x), _ptr(out), B * H,
+                                  float(theta_base), _stream(stream)))
+    return out
+
+
+def decode(q, k, v, q_pos0=None, causal=True, scale=None, split_len=512, out_fp32=False,
+           ws=None, out=None, lse=None, stream=None):
+    """Split-KV decoding (dfa_decode): q [B,Hq,T,d] bf16 at positions q_pos0 + t
+    (default: the last T positions of the cache) against k, v [B,Hkv,L,d]."""
+    _need_cuda(q, k, v)
+    B, Hq, T, d = q.shape
+    Hkv, L = k.shape[1], k.shape[2]
+    if q_pos0 is None:
+        q_pos0 = L - T
+    desc = make_desc(B, Hq, Hkv, L, d, causal=causal, scale=scale, o_fp32=out_fp32)
+    if ws is None:
+        n = int(lib().dfa_decode_workspace_size(ctypes.byref(desc), T, L, split_len))
+        if n == 0:
+            raise DfaError(1, "bad decode arguments")
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(B, Hq, T, d, dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    _check(lib().dfa_decode(ctypes.byref(desc), T, L, int(q_pos0), _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(out), _ptr(lse), split_len, _ptr(ws), ws.numel(),
+                            _stream(stream)))
+    return out, lse
+
+
+_copy_streams = {}
+
+
+def ring_fwd(q_chunks, k_chunks, v_chunks, partition, stripe=1, causal=True, scale=None,
+             overlap=True, outs=None, slots=None, ws=None, stream=None, copy_stream=None):
+    """The ring schedule on one GPU (dfa_ring_fwd): worker p holds chunk p of the
+    partition (q [B,Hq,n,d], k/v [B,Hkv,n,d] bf16, worker-major chunks); returns
+    [(o [B,Hq,n,d] fp32, lse [B,Hq,n] fp32)] per worker.  With overlap the K/V
+    hand-over runs on a second stream (copy_stream, or one kept per device)."""
+    P = len(q_chunks)
+    _need_cuda(*q_chunks, *k_chunks, *v_chunks)
+    B, Hq, n, d = q_chunks[0].shape
+    Hkv = k_chunks[0].shape[1]
+    dev = q_chunks[0].device
+    desc = make_desc(B, Hq, Hkv, n * P, d, causal=causal, scale=scale, P=P,
+                     partition=partition, stripe=stripe)
+    if outs is None:
+        outs = [(torch.empty(B, Hq, n, d, dtype=torch.float32, device=dev),
+                 torch.empty(B, Hq, n, dtype=torch.float32, device=dev)) for _ in range(P)]
+    if slots is None:
+        slots = [torch.empty(4 * B * Hkv * n * d, dtype=torch.bfloat16, device=dev)
+                 for _ in range(P)]
+    if ws is None:
+        ws = new_workspace(desc, OP_RING_FWD, dev)
+    if overlap and copy_stream is None:
+        copy_stream = _copy_streams.setdefault(dev, torch.cuda.Stream(dev))
+    arr = (RingWorker * P)(*[RingWorker(q.data_ptr(), k.data_ptr(), v.data_ptr(), sl.data_ptr(),
+                                        o.data_ptr(), l.data_ptr())
+                             for q, k, v, sl, (o, l) in zip(q_chunks, k_chunks, v_chunks, slots,
+                                                            outs)])
+    _check(lib().dfa_ring_fwd(ctypes.byref(desc), arr, _ptr(ws), ws.numel(), int(overlap),
+                              _stream(stream), _stream(copy_stream) if overlap else None))
+    return outs
 
 
 # ----------------------------------------------------------------------------

@@ -243,6 +243,26 @@ def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
     return o, lse
 
 
+def rope(x, pos, base: float = 10000.0, inverse: bool = False) -> np.ndarray:
+    """Rotary position embedding in fp64 (Striped Attention Guide, "Preserving
+    Rotary Position Embeddings"): the token at absolute position i is rotated by
+    R(Theta, i), the block-diagonal rotation that turns feature pair (2t, 2t+1)
+    by the angle i * theta_t, theta_t = base^(-2t/d); inverse applies R^T.
+    x: [..., N, d] (bf16 tensor or fp64 array); pos: [N] absolute positions."""
+    X = _f64(x)
+    d = X.shape[-1]
+    theta = base ** (-2.0 * np.arange(d // 2) / d)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    if inverse:
+        s = -s
+    a, b = X[..., 0::2], X[..., 1::2]
+    out = np.empty_like(X)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
 # ----------------------------------------------------------------------------
 # numpy twin: materialised scores, tiny shapes only
 # ----------------------------------------------------------------------------

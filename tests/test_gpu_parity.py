@@ -160,6 +160,35 @@ def test_partitioned_fused_matches_whole(orc, kind, shape):
     check_grad(dfa.permute(gv, P, kind, inverse=True), dv, "dV")
 
 
+@pytest.mark.parametrize("stripe", [64, 128])
+def test_block_striped_fused_matches_whole(orc, stripe):
+    """Block striping (Striped Attention Guide, "Mathematical Formulation of
+    Token Striping", blocks of `stripe` tokens dealt round-robin): permute ->
+    fused forward / backward over all worker pairs -> un-permute equals the
+    oracle's whole attention.  N = 3 * stripe * P leaves partial tiles."""
+    B, Hq, Hkv, d, P = 1, 2, 1, 128, 4
+    N = 3 * stripe * P
+    q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=11 + stripe)
+    O, L = orc.attn_fwd(q, k, v)
+    dq, dk, dv = orc.attn_bwd(q, k, v, do)
+    idx = torch.from_numpy(_perm_index(orc, "striped", N, P, stripe))
+    perm = [dfa.permute(t.cuda(), P, "striped", stripe=stripe) for t in (q, k, v, do)]
+    for t, pt in zip((q, k, v, do), perm):
+        assert torch.equal(pt.cpu(), t[:, :, idx])
+    qp, kp, vp, dop = perm
+    kw = dict(P=P, partition="striped", stripe=stripe)
+    ws = dfa.new_workspace(dfa.desc_for(qp, kp, **kw), dfa.OP_BWD)
+    o, lse = dfa.attn_fwd(qp, kp, vp, ws=ws, **kw)
+    gq, gk, gv = dfa.attn_bwd(qp, kp, vp, o, dop, lse, ws=ws, **kw)
+    _status(ws)
+    inv = dict(inverse=True, stripe=stripe)
+    check_o(dfa.permute(o, P, "striped", **inv), O)
+    check_lse(dfa.permute(lse, P, "striped", **inv), L)
+    check_grad(dfa.permute(gq, P, "striped", **inv), dq, "dQ")
+    check_grad(dfa.permute(gk, P, "striped", **inv), dk, "dK")
+    check_grad(dfa.permute(gv, P, "striped", **inv), dv, "dV")
+
+
 @pytest.mark.parametrize("kind,stripe", [("contiguous", 1), ("balanced", 1), ("striped", 1),
                                          ("striped", 64)])
 def test_permute_roundtrip_bit_exact(orc, kind, stripe):

@@ -199,16 +199,18 @@ def test_merge_closed_forms(orc):
     assert np.abs(o5[0] - np.array([0.25, 0.75])).max() < 1e-15
 
 
-@pytest.mark.parametrize("kind", ["contiguous", "balanced", "striped"])
-def test_merge_identity_and_partition_invariance(orc, kind):
+@pytest.mark.parametrize("kind,stripe", [("contiguous", 1), ("balanced", 1), ("striped", 1),
+                                         ("striped", 4), ("striped", 8)])
+def test_merge_identity_and_partition_invariance(orc, kind, stripe):
     """Attention over the whole sequence == LSE-merge of the chunk-pair partials
     of every worker against every worker's keys, and the result, put back in
-    natural order, does not depend on the partition."""
+    natural order, does not depend on the partition (token or block striping,
+    Striped Attention Guide, "Mathematical Formulation of Token Striping")."""
     B, H, N, d, P = 1, 2, 64, 16, 4
     q, k, v, _ = make_qkvdo(B, H, H, N, d, seed=31)
     O, L = orc.attn_fwd(q, k, v, causal=True)
     n = N // P
-    pos = [orc.partition_pos(kind, N, P, p) for p in range(P)]
+    pos = [orc.partition_pos(kind, N, P, p, stripe) for p in range(P)]
     got_o = np.zeros_like(O)
     got_l = np.zeros_like(L)
     for p in range(P):
@@ -228,8 +230,9 @@ def test_merge_identity_and_partition_invariance(orc, kind):
     assert np.abs(got_l - L).max() < 1e-12
 
 
-@pytest.mark.parametrize("kind", ["contiguous", "balanced", "striped"])
-def test_chunk_backward_sums_to_full(orc, kind):
+@pytest.mark.parametrize("kind,stripe", [("contiguous", 1), ("balanced", 1), ("striped", 1),
+                                         ("striped", 4)])
+def test_chunk_backward_sums_to_full(orc, kind, stripe):
     """Sum over chunk pairs of each pair's gradient contribution (with the
     whole-sequence LSE and row constant) == the full backward."""
     B, Hq, Hkv, N, d, P = 1, 2, 1, 32, 8, 4
@@ -237,7 +240,7 @@ def test_chunk_backward_sums_to_full(orc, kind):
     dq, dk, dv = orc.attn_bwd(q, k, v, do, causal=True)
     O, L = orc.attn_fwd(q, k, v, causal=True)
     delta = (do.double().numpy() * O).sum(-1)
-    pos = [orc.partition_pos(kind, N, P, p) for p in range(P)]
+    pos = [orc.partition_pos(kind, N, P, p, stripe) for p in range(P)]
     gq, gk, gv = np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)
     for p in range(P):
         ip = torch.from_numpy(pos[p])
@@ -349,3 +352,44 @@ def test_tile_classes_closed_form(orc):
     for i in range(4):
         for j in range(4):
             assert cls[i, j] == (1 if i > j else (2 if i == j else 0))
+
+
+# ----------------------------------------------------------------------------
+# rotary position embedding (Striped Attention Guide, "Preserving Rotary
+# Position Embeddings")
+# ----------------------------------------------------------------------------
+def test_rope_position_zero_is_identity_and_norm_preserving(orc):
+    x = np.random.default_rng(1).standard_normal((2, 5, 64))
+    y = orc.rope(x, np.arange(5) * 1000)
+    assert np.abs(orc.rope(x[:, :1], [0]) - x[:, :1]).max() == 0.0
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-14)
+
+
+def test_rope_closed_forms_pin_pairing_and_frequencies(orc):
+    # d = 2: one pair, theta_0 = 1 -> rotation by the position itself
+    m = 7.0
+    assert np.allclose(orc.rope(np.array([[1.0, 0.0]]), [m]), [[np.cos(m), np.sin(m)]], atol=1e-15)
+    # d = 4, base 10000: pairs (0,1) turn by m, (2,3) by m/100; the second feature
+    # of a pair goes to (-sin, cos) of its pair only
+    e1 = np.array([[0.0, 1.0, 0.0, 0.0]])
+    e2 = np.array([[0.0, 0.0, 1.0, 0.0]])
+    assert np.allclose(orc.rope(e1, [m]), [[-np.sin(m), np.cos(m), 0, 0]], atol=1e-15)
+    assert np.allclose(orc.rope(e2, [m]), [[0, 0, np.cos(m / 100), np.sin(m / 100)]], atol=1e-15)
+
+
+def test_rope_inner_products_depend_only_on_distance(orc):
+    """q_i . k_j after rotation is a function of i - j (the invariance that
+    lets striped storage apply RoPE at global positions), also at 512K."""
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, 128))
+    k = rng.standard_normal((1, 128))
+    for i, j, t in ((5, 3, 100), (131071, 4096, 393000), (0, 0, 524287)):
+        a = (orc.rope(q, [i]) * orc.rope(k, [j])).sum()
+        b = (orc.rope(q, [i + t]) * orc.rope(k, [j + t])).sum()
+        assert abs(a - b) <= 1e-9 * (1 + abs(a))
+
+
+def test_rope_inverse_roundtrip(orc):
+    x = np.random.default_rng(3).standard_normal((3, 8, 128))
+    pos = np.arange(8) * 65537
+    assert np.abs(orc.rope(orc.rope(x, pos), pos, inverse=True) - x).max() < 1e-12
