@@ -84,6 +84,16 @@ typedef struct dfa_attn_desc {
     int32_t partition; /* DFA_PART_*                                       */
     int32_t stripe;    /* striped block size in tokens (1 = token stripes) */
     int32_t o_fp32;    /* dfa_attn_fwd output O: 0 bf16, 1 fp32            */
+    int32_t ndocs;     /* documents packed in the sequence (0: none)       */
+    const int64_t* doc_bounds; /* device, ndocs + 1 increasing positions:
+                                  document t is [doc_bounds[t],
+                                  doc_bounds[t+1]), doc_bounds[0] = 0,
+                                  doc_bounds[ndocs] = N.  A key is visible
+                                  only to queries of its own document
+                                  (Striped Attention Guide, "Document Packing
+                                  and Boundary Alignment"); causal masking
+                                  applies on top.  Not read by dfa_decode,
+                                  which rejects ndocs != 0.               */
 } dfa_attn_desc;
 
 /*

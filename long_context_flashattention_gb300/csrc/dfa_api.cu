@@ -126,6 +126,8 @@ dfa_status check_desc(const dfa_attn_desc* d, bool need_partition)
         return fail(DFA_ERR_INVALID_ARG, "scale must be positive and finite");
     if (d->causal != 0 && d->causal != 1)
         return fail(DFA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (d->ndocs < 0 || (d->ndocs > 0 && !d->doc_bounds))
+        return fail(DFA_ERR_INVALID_ARG, "ndocs must be >= 0, with doc_bounds when > 0");
     if (need_partition) {
         if (d->P < 1 || d->P > kMaxChunks)
             return fail(DFA_ERR_UNSUPPORTED, "P must be in [1, %d]", kMaxChunks);
@@ -325,6 +327,8 @@ dfa_status run_fwd(const dfa_attn_desc& d, const Layout& lay, const void* q, con
     p.scale = d.scale;
     p.scale_log2 = d.scale * 1.4426950408889634f;
     p.o_fp32 = o_fp32;
+    p.ndocs = d.ndocs;
+    p.docs = d.doc_bounds;
     p.units = build_units(lay.qmaps, fwd_rows_per_unit(), true);
     p.total_units = p.units.units_per_slice * p.BH;
     for (size_t i = 0; i < lay.qmaps.size(); ++i)
@@ -376,6 +380,8 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.scale = d.scale;
     p.scale_log2 = d.scale * 1.4426950408889634f;
     p.dkv_mode = dkv_mode;
+    p.ndocs = d.ndocs;
+    p.docs = d.doc_bounds;
     p.units = build_units(lay.kmaps, bwd_rows_per_unit(), false);
     p.total_units = p.units.units_per_slice * p.BHkv;
     for (size_t i = 0; i < lay.qmaps.size(); ++i)
@@ -767,6 +773,8 @@ dfa_status dfa_decode(const dfa_attn_desc* desc, int32_t T, int64_t L, int64_t q
         return s;
     if (T < 1 || L < 1 || L >= INT32_MAX || q_pos0 < 0)
         return fail(DFA_ERR_INVALID_ARG, "need T >= 1, 1 <= L < 2^31, q_pos0 >= 0");
+    if (desc->ndocs != 0)
+        return fail(DFA_ERR_UNSUPPORTED, "dfa_decode takes no document bounds");
     if (split_len < 64 || split_len % 64 != 0)
         return fail(DFA_ERR_INVALID_ARG, "split_len must be a positive multiple of 64");
     const int G = desc->Hq / desc->Hkv;

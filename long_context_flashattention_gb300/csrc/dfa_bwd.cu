@@ -97,31 +97,45 @@ struct Cfg {
     __host__ __device__ static constexpr uint32_t cDP(int b) { return 2 * D + 128 * b + 64; }
 };
 
-// Query tiles of chunk p that the unit's key rows can see: [i0, nqt); tiles
-// with index >= ifull (and complete) need no mask.
+// Query tiles of chunk p that the unit's key rows can see: [i0, i1); tiles in
+// [if0, if1) see every key row (no mask).  A key at position y is seen by the
+// queries at positions [causal ? y : doc_lo(y), doc_hi(y) - 1] (its document;
+// everything without documents), an interval of each query chunk.  Union over
+// the unit's keys: [lower(y_min), doc_hi(y_max) - 1]; intersection:
+// [lower(y_max), doc_hi(y_min) - 1], and only when all keys share a document.
 struct QRange {
-    int32_t p, i0, nqt, ifull;
+    int32_t p, i0, i1, if0, if1;
 };
 
 __device__ __forceinline__ QRange q_range(const BwdParams& pr, const Unit& un, int s)
 {
     QRange r;
     r.p = pr.ring ? (un.chunk + s) % pr.nq : s;
-    r.nqt = ceil_div(pr.chunk_q, BQ);
-    if (!pr.causal) {
+    const int32_t nqt = ceil_div(pr.chunk_q, BQ);
+    if (!pr.causal && pr.ndocs == 0) {
         r.i0 = 0;
-        r.ifull = 0;
+        r.i1 = nqt;
+        r.if0 = 0;
+        r.if1 = pr.chunk_q / BQ;
         return r;
     }
     const DevMap& km = pr.kmap[un.chunk];
     const DevMap& qm = pr.qmap[r.p];
     const int32_t pk_min = map_pos(km, un.row0);
     const int32_t pk_max = map_pos(km, un.row0 + un.nvalid - 1);
-    // first query row whose position is >= pk (positions increase along the chunk)
-    const int32_t first_vis = map_count_le(qm, pk_min - 1);
-    const int32_t first_full = map_count_le(qm, pk_max - 1);
-    r.i0 = first_vis >= pr.chunk_q ? r.nqt : first_vis / BQ;
-    r.ifull = ceil_div(first_full, BQ);
+    int32_t lo_min, hi_min, lo_max, hi_max;
+    doc_range(pr.docs, pr.ndocs, pk_min, lo_min, hi_min);
+    doc_range(pr.docs, pr.ndocs, pk_max, lo_max, hi_max);
+    const int32_t first_vis = map_count_le(qm, (pr.causal ? pk_min : lo_min) - 1);
+    const int32_t end_vis = map_count_le(qm, hi_max - 1);
+    const int32_t first_full = map_count_le(qm, (pr.causal ? pk_max : lo_max) - 1);
+    const int32_t end_full = lo_max <= pk_min ? map_count_le(qm, hi_min - 1) : 0;
+    r.i0 = first_vis / BQ;
+    r.i1 = ceil_div(end_vis, BQ);
+    if (r.i1 < r.i0)
+        r.i1 = r.i0;
+    r.if0 = ceil_div(first_full, BQ);
+    r.if1 = end_full / BQ;
     return r;
 }
 
@@ -130,7 +144,7 @@ __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& u
     int32_t t = 0;
     for (int s = 0; s < pr.nq; ++s) {
         QRange r = q_range(pr, un, s);
-        t += r.nqt - r.i0;
+        t += r.i1 - r.i0;
     }
     return t * pr.G;
 }
@@ -196,7 +210,7 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
             const int slice_q = b * p.Hq + hk * p.G + g;
             for (int s = 0; s < p.nq; ++s) {
                 QRange qr = q_range(p, un, s);
-                for (int i = qr.i0; i < qr.nqt; ++i, ++qc) {
+                for (int i = qr.i0; i < qr.i1; ++i, ++qc) {
                     const int st = qc % C::kQStages;
                     const uint32_t use = qc / C::kQStages;
                     if (lane == 0 && use > 0 &&
@@ -388,12 +402,16 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
             for (int g = 0; g < p.G; ++g) {
                 for (int s = 0; s < p.nq; ++s) {
                     QRange qr = q_range(p, un, s);
-                    if (qr.i0 >= qr.nqt)
+                    if (qr.i0 >= qr.i1)
                         continue;
-                    // first query row of chunk qr.p that sees this key row
+                    // query rows [qv, qe) of chunk qr.p see this key row
+                    int32_t dlo, dhi;
+                    doc_range(p.docs, p.ndocs, pk, dlo, dhi);
                     const int32_t qv =
-                        !kvalid ? 0x7fffffff : (p.causal ? map_count_le(p.qmap[qr.p], pk - 1) : 0);
-                    for (int i = qr.i0; i < qr.nqt; ++i, ++n) {
+                        !kvalid ? 0x7fffffff
+                                : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);
+                    const int32_t qe = map_count_le(p.qmap[qr.p], dhi - 1);
+                    for (int i = qr.i0; i < qr.i1; ++i, ++n) {
                         const int st = n % C::kQStages;
                         const int b = n & 1;
                         if (!mbar_wait(&bar[C::QFULL + st], (n / C::kQStages) & 1, w, 70))
@@ -404,7 +422,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         uint32_t sr[32], dr[32];
                         tmem_ld32(tl + C::cS(b) + 32 * h, sr);
                         tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
-                        const bool full = (i >= qr.ifull) && ((i + 1) * BQ <= p.chunk_q) &&
+                        const bool full = (i >= qr.if0 && i < qr.if1) &&
                                           un.nvalid == kKvRows;
                         const int qbase = i * BQ + 32 * h;
                         tmem_ld_wait();
@@ -427,8 +445,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                             float p0 = ex2(a0), p1 = ex2(a1);
                             if (!full) {
                                 const int q = qbase + 2 * j;
-                                p0 = (q >= qv && q < p.chunk_q) ? p0 : 0.f;
-                                p1 = (q + 1 >= qv && q + 1 < p.chunk_q) ? p1 : 0.f;
+                                p0 = (q >= qv && q < qe) ? p0 : 0.f;
+                                p1 = (q + 1 >= qv && q + 1 < qe) ? p1 : 0.f;
                             }
                             sr[2 * j] = __float_as_uint(p0);
                             sr[2 * j + 1] = __float_as_uint(p1);
@@ -548,7 +566,7 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
                 QRange qr = q_range(p, un, s);
                 float* base =
                     p.dq_acc + ((size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q) * D + L;
-                for (int i = qr.i0; i < qr.nqt; ++i, ++n) {
+                for (int i = qr.i0; i < qr.i1; ++i, ++n) {
                     const int b = n & 1;
                     if (!mbar_wait(&bar[C::DQFULL + b], (n >> 1) & 1, w, 80))
                         return;

@@ -58,35 +58,50 @@ struct Cfg {
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;  // + tmem slot, flag, align
 };
 
-// Per-(unit, kv-chunk step) tile counts: visible tiles [0, jv), of which
-// [0, jf) need no mask.
+// Per-(unit, kv-chunk step) tiles: visible tiles [j0, jv), of which
+// [jf0, jf) need no mask.  A row at position x sees the keys at positions
+// [doc_lo(x), causal ? x : doc_hi(x) - 1] (its document; everything without
+// documents), an interval of each key chunk because positions increase along
+// a chunk.  Union over the unit's rows: [doc_lo(x_min), upper(x_max)];
+// intersection: [doc_lo(x_max), upper(x_min)].
 struct StepTiles {
-    int32_t c, jv, jf;
+    int32_t c, j0, jv, jf0, jf;
 };
 
 __device__ __forceinline__ StepTiles step_tiles(const FwdParams& p, const Unit& un, int s)
 {
     StepTiles r;
     r.c = p.ring ? (un.chunk - s + p.nkv) % p.nkv : s;
-    if (!p.causal) {
+    const DevMap& km = p.kmap[r.c];
+    if (!p.causal && p.ndocs == 0) {
+        r.j0 = 0;
+        r.jf0 = 0;
         r.jv = ceil_div(p.chunk_k, 128);
         r.jf = p.chunk_k / 128;
         return r;
     }
     const DevMap& qm = p.qmap[un.chunk];
-    int32_t pq_min = map_pos(qm, un.row0);
-    int32_t pq_max = map_pos(qm, un.row0 + un.nvalid - 1);
-    const DevMap& km = p.kmap[r.c];
-    r.jv = ceil_div(map_count_le(km, pq_max), 128);
-    r.jf = map_count_le(km, pq_min) / 128;
+    const int32_t pq_min = map_pos(qm, un.row0);
+    const int32_t pq_max = map_pos(qm, un.row0 + un.nvalid - 1);
+    int32_t lo_min, hi_min, lo_max, hi_max;
+    doc_range(p.docs, p.ndocs, pq_min, lo_min, hi_min);
+    doc_range(p.docs, p.ndocs, pq_max, lo_max, hi_max);
+    const int32_t up_max = p.causal ? pq_max : hi_max - 1;
+    const int32_t up_min = p.causal ? pq_min : hi_min - 1;
+    r.j0 = map_count_le(km, lo_min - 1) / 128;
+    r.jv = ceil_div(map_count_le(km, up_max), 128);
+    r.jf0 = ceil_div(map_count_le(km, lo_max - 1), 128);
+    r.jf = map_count_le(km, up_min) / 128;
     return r;
 }
 
 __device__ __forceinline__ int32_t unit_tiles(const FwdParams& p, const Unit& un)
 {
     int32_t t = 0;
-    for (int s = 0; s < p.nkv; ++s)
-        t += step_tiles(p, un, s).jv;
+    for (int s = 0; s < p.nkv; ++s) {
+        const StepTiles st = step_tiles(p, un, s);
+        t += st.jv > st.j0 ? st.jv - st.j0 : 0;
+    }
     return t;
 }
 
@@ -186,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++qc;
                     for (int s = 0; s < p.nkv; ++s) {
                         StepTiles st = step_tiles(p, un, s);
-                        for (int j = 0; j < st.jv; ++j) {
+                        for (int j = st.j0; j < st.jv; ++j) {
                             const int ks = kc % C::kStages;
                             const uint32_t n = kc / C::kStages;
                             const int krow = st.c * p.chunk_k + j * 128;
@@ -313,11 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (total > 0) {
                 for (int s = 0; s < p.nkv; ++s) {
                     StepTiles st = step_tiles(p, un, s);
-                    if (st.jv == 0)
+                    if (st.jv <= st.j0)
                         continue;
+                    // this row's visible keys of the chunk: rows [lo, cnt)
+                    int32_t dlo, dhi;
+                    doc_range(p.docs, p.ndocs, pq, dlo, dhi);
                     const int32_t cnt =
-                        !valid ? 0 : (p.causal ? map_count_le(p.kmap[st.c], pq) : p.chunk_k);
-                    for (int j = 0; j < st.jv; ++j) {
+                        !valid ? 0 : map_count_le(p.kmap[st.c], p.causal ? pq : dhi - 1);
+                    const int32_t lo = map_count_le(p.kmap[st.c], dlo - 1);
+                    for (int j = st.j0; j < st.jv; ++j) {
                         if (!mbar_wait(&bar[C::SFULL + t], sc & 1, wctx, 30 + t))
                             goto softmax_done;
                         ++sc;
@@ -336,11 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 128; ++i)
                             sv[i] = __uint_as_float(r[i]);
-                        if (j >= st.jf || !valid) {
-                            const int nv = cnt - j * 128;
+                        if (j < st.jf0 || j >= st.jf || !valid) {
+                            const int nv = cnt - j * 128, n0 = lo - j * 128;
 #pragma unroll
                             for (int i = 0; i < 128; ++i)
-                                sv[i] = (i < nv) ? sv[i] : -INFINITY;
+                                sv[i] = (i >= n0 && i < nv) ? sv[i] : -INFINITY;
                         }
                         // row max, two new values per 3-input max
                         float mx = fmaxf(sv[0], sv[1]);

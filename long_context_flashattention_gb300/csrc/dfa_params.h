@@ -66,6 +66,30 @@ DFA_HD int32_t map_count_le(const DevMap& m, int32_t x)
 
 DFA_HD int32_t ceil_div(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
+// Packed documents: positions [bounds[t], bounds[t+1]), t < ndocs, form
+// document t.  doc_range gives the document [lo, hi) of position x; without
+// documents (ndocs = 0) it is the whole line.
+constexpr int32_t kPosLo = INT32_MIN + 2, kPosHi = INT32_MAX - 1;
+
+DFA_HD void doc_range(const int64_t* bounds, int32_t ndocs, int32_t x, int32_t& lo, int32_t& hi)
+{
+    if (ndocs <= 0) {
+        lo = kPosLo;
+        hi = kPosHi;
+        return;
+    }
+    int32_t a = 0, c = ndocs;  // largest t with bounds[t] <= x
+    while (c - a > 1) {
+        const int32_t mid = (a + c) / 2;
+        if (bounds[mid] <= x)
+            a = mid;
+        else
+            c = mid;
+    }
+    lo = (int32_t)bounds[a];
+    hi = (int32_t)bounds[a + 1];
+}
+
 // Work units.  The rows of every chunk are cut into segments (runs of rows
 // inside one map segment) and each segment into units of `rows_per_unit`
 // rows; units are replicated over the BH (batch x head) slices.  Inside a
@@ -167,6 +191,8 @@ struct FwdParams {
     float scale, scale_log2;
     int32_t total_units;
     int32_t o_fp32;
+    int32_t ndocs;               // packed documents (0: none)
+    const int64_t* docs;         // [ndocs + 1] cumulative positions (device)
     UnitTable units;
     DevMap qmap[kMaxChunks];
     DevMap kmap[kMaxChunks];
@@ -187,6 +213,8 @@ struct BwdParams {
     float scale, scale_log2;
     int32_t total_units;
     int32_t dkv_mode;            // 0: write bf16 dK/dV; 1: accumulate into fp32
+    int32_t ndocs;               // packed documents (0: none)
+    const int64_t* docs;         // [ndocs + 1] cumulative positions (device)
     UnitTable units;
     DevMap qmap[kMaxChunks];
     DevMap kmap[kMaxChunks];

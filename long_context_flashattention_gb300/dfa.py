@@ -34,7 +34,8 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("N", ctypes.c_int64), ("d", ctypes.c_int32), ("causal", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("P", ctypes.c_int32), ("partition", ctypes.c_int32),
-                ("stripe", ctypes.c_int32), ("o_fp32", ctypes.c_int32)]
+                ("stripe", ctypes.c_int32), ("o_fp32", ctypes.c_int32),
+                ("ndocs", ctypes.c_int32), ("doc_bounds", ctypes.c_void_p)]
 
 
 class PosMap(ctypes.Structure):
@@ -128,11 +129,20 @@ def _stream(stream=None):
 
 
 def make_desc(B, Hq, Hkv, N, d, causal=True, scale=None, P=1, partition="contiguous",
-              stripe=1, o_fp32=False) -> AttnDesc:
+              stripe=1, o_fp32=False, docs=None) -> AttnDesc:
+    """docs: None, or an int64 CUDA tensor of ndocs + 1 cumulative document
+    bounds in global positions (kept alive by the descriptor)."""
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    return AttnDesc(B, Hq, Hkv, N, d, int(causal), float(scale), P, PARTITIONS[partition],
-                    stripe, int(o_fp32))
+    nd, ptr = 0, None
+    if docs is not None:
+        if not docs.is_cuda or docs.dtype != torch.int64 or docs.dim() != 1 or docs.numel() < 2:
+            raise ValueError("docs must be a 1-D int64 CUDA tensor of >= 2 bounds")
+        nd, ptr = docs.numel() - 1, docs.data_ptr()
+    desc = AttnDesc(B, Hq, Hkv, N, d, int(causal), float(scale), P, PARTITIONS[partition],
+                    stripe, int(o_fp32), nd, ptr)
+    desc._docs = docs
+    return desc
 
 
 def desc_for(q, k, **kw) -> AttnDesc:
@@ -162,13 +172,13 @@ def _need_cuda(*ts):
 # whole-sequence attention
 # ----------------------------------------------------------------------------
 def attn_fwd(q, k, v, causal=True, scale=None, P=1, partition="contiguous", stripe=1,
-             o_fp32=False, ws=None, out=None, lse=None, stream=None):
+             o_fp32=False, ws=None, out=None, lse=None, stream=None, docs=None):
     """Attention forward.  q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16, rows in the
     worker-major order of the partition (natural order for contiguous).
     Returns (O, LSE)."""
     _need_cuda(q, k, v)
     desc = desc_for(q, k, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe,
-                    o_fp32=o_fp32)
+                    o_fp32=o_fp32, docs=docs)
     B, Hq, N, d = q.shape
     if out is None:
         out = torch.empty(B, Hq, N, d, dtype=torch.float32 if o_fp32 else torch.bfloat16,
@@ -183,10 +193,11 @@ def attn_fwd(q, k, v, causal=True, scale=None, P=1, partition="contiguous", stri
 
 
 def attn_bwd(q, k, v, o, dout, lse, causal=True, scale=None, P=1, partition="contiguous",
-             stripe=1, ws=None, dq=None, dk=None, dv=None, stream=None):
+             stripe=1, ws=None, dq=None, dk=None, dv=None, stream=None, docs=None):
     """Recomputation backward.  Returns (dQ, dK, dV) in bf16."""
     _need_cuda(q, k, v, o, dout, lse)
-    desc = desc_for(q, k, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe)
+    desc = desc_for(q, k, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe,
+                    docs=docs)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -234,12 +245,12 @@ def partition_map(N, P, p, partition="contiguous", stripe=1) -> PosMap:
 
 
 def chunk_fwd(q, k, v, qmap: PosMap, kvmap: PosMap, causal=True, scale=None, ws=None,
-              o_part=None, lse_part=None, stream=None):
+              o_part=None, lse_part=None, stream=None, docs=None):
     """Partial (O fp32, LSE) of one chunk pair at the given global positions."""
     _need_cuda(q, k, v)
     B, Hq, Lq, d = q.shape
     Lk = k.shape[2]
-    desc = make_desc(B, Hq, k.shape[1], max(Lq, Lk), d, causal=causal, scale=scale)
+    desc = make_desc(B, Hq, k.shape[1], max(Lq, Lk), d, causal=causal, scale=scale, docs=docs)
     pair = ChunkPair(qmap, kvmap)
     if o_part is None:
         o_part = torch.empty(B, Hq, Lq, d, dtype=torch.float32, device=q.device)
@@ -254,12 +265,12 @@ def chunk_fwd(q, k, v, qmap: PosMap, kvmap: PosMap, causal=True, scale=None, ws=
 
 
 def chunk_bwd(q, k, v, o, dout, lse, qmap: PosMap, kvmap: PosMap, dq_acc, dk_acc, dv_acc,
-              delta=None, causal=True, scale=None, ws=None, stream=None):
+              delta=None, causal=True, scale=None, ws=None, stream=None, docs=None):
     """Accumulate one chunk pair's gradient contribution (fp32 accumulators)."""
     _need_cuda(q, k, v, dout, lse, dq_acc, dk_acc, dv_acc)
     B, Hq, Lq, d = q.shape
     Lk = k.shape[2]
-    desc = make_desc(B, Hq, k.shape[1], Lq, d, causal=causal, scale=scale)
+    desc = make_desc(B, Hq, k.shape[1], Lq, d, causal=causal, scale=scale, docs=docs)
     pair = ChunkPair(qmap, kvmap)
     if ws is None:
         ws = new_workspace(desc, OP_CHUNK_BWD, q.device)

@@ -75,6 +75,8 @@ def lib():
         L.orc_tile_classes.argtypes = [i32, i64, i32, i32, i32, i32, i32, i32, vp]
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
+        L.orc_set_docs.restype = None
+        L.orc_set_docs.argtypes = [vp, i32]
         _lib = L
     return _lib
 
@@ -142,12 +144,28 @@ def tile_classes(kind: str, N: int, P: int, p: int, w: int, tm: int, tn: int,
 # ----------------------------------------------------------------------------
 # attention
 # ----------------------------------------------------------------------------
+class _Docs:
+    """Document bounds for the duration of one oracle call (``docs``: the
+    cumulative positions bounds[0..ndocs]; None = no documents)."""
+
+    def __init__(self, docs):
+        self.b = None if docs is None else np.ascontiguousarray(np.asarray(docs, dtype=np.int64))
+
+    def __enter__(self):
+        if self.b is not None:
+            lib().orc_set_docs(_ptr(self.b), len(self.b) - 1)
+
+    def __exit__(self, *a):
+        lib().orc_set_docs(None, 0)
+
+
 def attn_fwd(q, k, v, causal=True, scale=None, qpos=None, kpos=None, rows=None,
-             nthreads=0):
+             nthreads=0, docs=None):
     """Forward attention (fp64).  q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] bf16.
 
     Returns (O [B,Hq,Lq,d] or [len(rows),d], LSE [B,Hq,Lq] or [len(rows)]).
-    ``rows`` are flat indices (b*Hq + h)*Lq + i.
+    ``rows`` are flat indices (b*Hq + h)*Lq + i.  ``docs``: cumulative document
+    bounds in positions (keys outside the query's document are masked).
     """
     (qb, kb, vb), f64 = _inputs(q, k, v)
     B, Hq, Lq, d = qb.shape
@@ -161,18 +179,19 @@ def attn_fwd(q, k, v, causal=True, scale=None, qpos=None, kpos=None, rows=None,
     o = np.zeros((len(rows), d), dtype=np.float64)
     lse = np.zeros(len(rows), dtype=np.float64)
     qp, kp = _pos(qpos), _pos(kpos)
-    lib().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), f64, B, Hq, Hkv, Lq, Lk, d,
-                            int(causal), float(scale),
-                            _ptr(qp) if qp is not None else None,
-                            _ptr(kp) if kp is not None else None,
-                            len(rows), _ptr(rows), _ptr(o), _ptr(lse), nthreads)
+    with _Docs(docs):
+        lib().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), f64, B, Hq, Hkv, Lq, Lk, d,
+                                int(causal), float(scale),
+                                _ptr(qp) if qp is not None else None,
+                                _ptr(kp) if kp is not None else None,
+                                len(rows), _ptr(rows), _ptr(o), _ptr(lse), nthreads)
     if full:
         return o.reshape(B, Hq, Lq, d), lse.reshape(B, Hq, Lq)
     return o, lse
 
 
 def attn_bwd(q, k, v, dout, causal=True, scale=None, qpos=None, kpos=None,
-             lse=None, delta=None, nthreads=0):
+             lse=None, delta=None, nthreads=0, docs=None):
     """Full backward (fp64): returns dQ, dK, dV.
 
     With ``lse``/``delta`` given, returns the contribution of the keys given to
@@ -189,17 +208,18 @@ def attn_bwd(q, k, v, dout, causal=True, scale=None, qpos=None, kpos=None,
     qp, kp = _pos(qpos), _pos(kpos)
     ls = None if lse is None else np.ascontiguousarray(np.asarray(lse, dtype=np.float64))
     de = None if delta is None else np.ascontiguousarray(np.asarray(delta, dtype=np.float64))
-    lib().orc_attn_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), f64, B, Hq, Hkv, Lq, Lk, d,
-                       int(causal), float(scale),
-                       _ptr(qp) if qp is not None else None,
-                       _ptr(kp) if kp is not None else None,
-                       _ptr(ls) if ls is not None else None,
-                       _ptr(de) if de is not None else None,
-                       _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
+    with _Docs(docs):
+        lib().orc_attn_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), f64, B, Hq, Hkv, Lq, Lk, d,
+                           int(causal), float(scale),
+                           _ptr(qp) if qp is not None else None,
+                           _ptr(kp) if kp is not None else None,
+                           _ptr(ls) if ls is not None else None,
+                           _ptr(de) if de is not None else None,
+                           _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
     return dq, dk, dv
 
 
-def attn_bwd_q_rows(q, k, v, dout, rows, causal=True, scale=None, nthreads=0):
+def attn_bwd_q_rows(q, k, v, dout, rows, causal=True, scale=None, nthreads=0, docs=None):
     """dQ of selected rows (fp64) plus each row's LSE and row constant D."""
     (qb, kb, vb, db), f64 = _inputs(q, k, v, dout)
     B, Hq, Lq, d = qb.shape
@@ -210,9 +230,10 @@ def attn_bwd_q_rows(q, k, v, dout, rows, causal=True, scale=None, nthreads=0):
     dq = np.zeros((len(rows), d))
     lse = np.zeros(len(rows))
     rc = np.zeros(len(rows))
-    lib().orc_attn_bwd_q_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), f64, B, Hq, Hkv, Lq, Lk,
-                              d, int(causal), float(scale), len(rows), _ptr(rows),
-                              _ptr(dq), _ptr(lse), _ptr(rc), nthreads)
+    with _Docs(docs):
+        lib().orc_attn_bwd_q_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), f64, B, Hq, Hkv, Lq,
+                                  Lk, d, int(causal), float(scale), len(rows), _ptr(rows),
+                                  _ptr(dq), _ptr(lse), _ptr(rc), nthreads)
     return dq, lse, rc
 
 

@@ -61,6 +61,49 @@ static inline double ld(const void* p, int64_t i, int f64)
 }
 
 /* ---------------------------------------------------------------------------
+ * Document masking (Striped Attention Guide, "Document Packing and Boundary
+ * Alignment": documents concatenated into one sequence must not attend to
+ * each other; boundaries by cumulative document indexing).  Reading: the
+ * documents are the position ranges [bounds[t], bounds[t+1]), t < ndocs; a
+ * key is visible to a query only when both positions lie in the same range
+ * (and, when causal, the key's position is not after the query's).  Set once
+ * with orc_set_docs (ndocs = 0: no documents); it applies to
+ * orc_attn_fwd_rows, orc_attn_bwd and orc_attn_bwd_q_rows.
+ * ------------------------------------------------------------------------- */
+static int64_t* g_docs = NULL;
+static int g_ndocs = 0;
+
+void orc_set_docs(const int64_t* bounds, int ndocs)
+{
+    free(g_docs);
+    g_docs = NULL;
+    g_ndocs = 0;
+    if (ndocs > 0 && bounds) {
+        g_docs = (int64_t*)malloc(sizeof(int64_t) * (size_t)(ndocs + 1));
+        memcpy(g_docs, bounds, sizeof(int64_t) * (size_t)(ndocs + 1));
+        g_ndocs = ndocs;
+    }
+}
+
+/* index of the document holding position x (-1 outside every document) */
+static int doc_of(int64_t x)
+{
+    for (int t = 0; t < g_ndocs; ++t)
+        if (g_docs[t] <= x && x < g_docs[t + 1])
+            return t;
+    return -1;
+}
+
+static int visible(int causal, int64_t pi, int64_t pj)
+{
+    if (causal && pj > pi)
+        return 0;
+    if (g_ndocs > 0 && doc_of(pi) != doc_of(pj))
+        return 0;
+    return 1;
+}
+
+/* ---------------------------------------------------------------------------
  * Sequence partitions.
  *
  * kind 0, contiguous: worker p owns tokens [p*N/P, (p+1)*N/P)
@@ -170,7 +213,7 @@ void orc_attn_fwd_rows(const void* q, const void* k, const void* v, int f64,
             double m = -INFINITY;
             for (int64_t j = 0; j < Lk; ++j) {
                 int64_t pj = kpos ? kpos[j] : j;
-                if (causal && pj > pi) {
+                if (!visible(causal, pi, pj)) {
                     s[j] = -INFINITY;
                     continue;
                 }
@@ -257,7 +300,7 @@ void orc_attn_bwd(const void* q, const void* k, const void* v, const void* dout,
                     double m = -INFINITY;
                     for (int64_t j = 0; j < Lk; ++j) {
                         int64_t pj = kpos ? kpos[j] : j;
-                        if (causal && pj > pi) {
+                        if (!visible(causal, pi, pj)) {
                             s[j] = -INFINITY;
                             continue;
                         }
@@ -356,7 +399,7 @@ void orc_attn_bwd_q_rows(const void* q, const void* k, const void* v,
                 dqr[c] = 0.0;
             double m = -INFINITY;
             for (int64_t j = 0; j < Lk; ++j) {
-                if (causal && j > i) {
+                if (!visible(causal, i, j)) {
                     s[j] = -INFINITY;
                     continue;
                 }
@@ -401,7 +444,7 @@ void orc_attn_bwd_q_rows(const void* q, const void* k, const void* v,
 
 /* ---------------------------------------------------------------------------
  * dK and dV for selected key rows of one (b, kv-head) group, causal, natural
- * order.  First the full softmax statistics (LSE_i and sum_l P_il dP_il) of
+ * order, without documents (orc_set_docs does not apply here).  First the full softmax statistics (LSE_i and sum_l P_il dP_il) of
  * every query row of the group's G heads are computed from the definition;
  * then, for each selected key j, dV_j = sum_{h,i>=j} P_ij dO_i and
  * dK_j = scale sum_{h,i>=j} dS_ij q_i.  krows[r] is the key index j; outputs

@@ -393,3 +393,56 @@ def test_rope_inverse_roundtrip(orc):
     x = np.random.default_rng(3).standard_normal((3, 8, 128))
     pos = np.arange(8) * 65537
     assert np.abs(orc.rope(orc.rope(x, pos), pos, inverse=True) - x).max() < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# document masking (Striped Attention Guide, "Document Packing and Boundary
+# Alignment")
+# ----------------------------------------------------------------------------
+DOC_BOUNDS = [0, 5, 6, 20, 41, 48]   # ragged documents, one of a single token
+
+
+def test_docs_equal_independent_attention_per_document(orc):
+    """Attention over packed documents == each document's causal attention on
+    its own (forward and all gradients), concatenated."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 48, 8
+    q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=71)
+    O, L = orc.attn_fwd(q, k, v, docs=DOC_BOUNDS)
+    dq, dk, dv = orc.attn_bwd(q, k, v, do, docs=DOC_BOUNDS)
+    for a, b in zip(DOC_BOUNDS[:-1], DOC_BOUNDS[1:]):
+        s = slice(a, b)
+        o1, l1 = orc.attn_fwd(q[:, :, s], k[:, :, s], v[:, :, s])
+        g1 = orc.attn_bwd(q[:, :, s], k[:, :, s], v[:, :, s], do[:, :, s])
+        assert np.abs(O[:, :, s] - o1).max() < 1e-13
+        assert np.abs(L[:, :, s] - l1).max() < 1e-13
+        for x, y in zip((dq, dk, dv), g1):
+            assert np.abs(x[:, :, s] - y).max() < 1e-13
+
+
+def test_docs_single_document_is_plain_attention(orc):
+    q, k, v, do = make_qkvdo(1, 2, 2, 24, 8, seed=72)
+    O, L = orc.attn_fwd(q, k, v, docs=[0, 24])
+    O0, L0 = orc.attn_fwd(q, k, v)
+    assert np.array_equal(O, O0) and np.array_equal(L, L0)
+    # and the setting does not leak into later calls
+    O1, _ = orc.attn_fwd(q, k, v)
+    assert np.array_equal(O1, O0)
+
+
+def test_docs_with_partition_positions(orc):
+    """Documents are ranges of GLOBAL positions: a striped partition's chunk
+    pairs, merged, reproduce the document-masked whole attention."""
+    B, H, N, d, P = 1, 2, 48, 8, 4
+    q, k, v, _ = make_qkvdo(B, H, H, N, d, seed=73)
+    O, L = orc.attn_fwd(q, k, v, docs=DOC_BOUNDS)
+    pos = [orc.partition_pos("striped", N, P, p) for p in range(P)]
+    for p in range(P):
+        parts_o, parts_l = [], []
+        for w in range(P):
+            po, pl = orc.attn_fwd(q[:, :, pos[p]], k[:, :, pos[w]], v[:, :, pos[w]],
+                                  qpos=pos[p], kpos=pos[w], docs=DOC_BOUNDS)
+            parts_o.append(po.reshape(-1, d))
+            parts_l.append(pl.reshape(-1))
+        mo, ml = orc.lse_merge(np.stack(parts_o), np.stack(parts_l))
+        assert np.abs(mo.reshape(B, H, -1, d) - O[:, :, pos[p]]).max() < 1e-12
+        assert np.abs(ml.reshape(B, H, -1) - L[:, :, pos[p]]).max() < 1e-12
