@@ -299,6 +299,15 @@ dfa_status check_ws(void* ws, size_t have, size_t need)
 // forward / backward launches over a layout of nq query chunks and nkv kv
 // chunks (shared by the whole-sequence and chunk-pair calls)
 // ----------------------------------------------------------------------------
+// Above this many query rows per head the backward cuts the query side into
+// blocks of about kBwdBlockRows rows (same local tile range in every query
+// chunk): the units running at one time then share one block's Q, dO and dQ
+// rows (about 32 MB) in L2 instead of a whole head's, and dK / dV are summed
+// over the blocks in fp32.
+constexpr int64_t kBwdBlockAbove = 65536, kBwdBlockRows = 32768;
+
+bool bwd_blocked(int64_t q_rows_per_head) { return q_rows_per_head > kBwdBlockAbove; }
+
 struct Layout {
     std::vector<dfa_pos_map> qmaps, kmaps;
     int64_t chunk_q, chunk_k;
@@ -383,7 +392,18 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.ndocs = d.ndocs;
     p.docs = d.doc_bounds;
     p.units = build_units(lay.kmaps, bwd_rows_per_unit(), false);
-    p.total_units = p.units.units_per_slice * p.BHkv;
+    const int bq = bwd_query_rows_per_step();
+    const int64_t nqt = (lay.chunk_q + bq - 1) / bq;
+    p.nqblk = 1;
+    p.qblk_tiles = (int32_t)nqt;
+    if (bwd_blocked(Lq)) {
+        const int64_t rows_per_chunk = std::max<int64_t>(bq, kBwdBlockRows / (int64_t)lay.qmaps.size());
+        p.qblk_tiles = (int32_t)std::max<int64_t>(1, rows_per_chunk / bq);
+        p.nqblk = (int32_t)((nqt + p.qblk_tiles - 1) / p.qblk_tiles);
+    }
+    if ((int64_t)p.units.units_per_slice * p.BHkv * p.nqblk >= INT32_MAX)
+        return fail(DFA_ERR_UNSUPPORTED, "too many backward work units");
+    p.total_units = p.units.units_per_slice * p.BHkv * p.nqblk;
     for (size_t i = 0; i < lay.qmaps.size(); ++i)
         p.qmap[i] = to_dev(lay.qmaps[i]);
     for (size_t i = 0; i < lay.kmaps.size(); ++i)
@@ -395,7 +415,6 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.timeout_ns = kDefaultTimeoutNs;
     if (p.total_units == 0)
         return DFA_OK;
-    const int bq = bwd_query_rows_per_step();
     CUtensorMap tq, tk, tv, tdo, tal, tad;
     dfa_status s;
     const int64_t BHq = (int64_t)d.B * d.Hq, BHkv = (int64_t)d.B * d.Hkv;
@@ -449,11 +468,13 @@ dfa_status check_ptrs(std::initializer_list<const void*> ps)
 }
 
 // Backward workspace: status word, fp32 dQ accumulator, -LSE/scale and -D
-// records (32 bytes a row each).
+// records (32 bytes a row each), and with query blocking fp32 dK and dV.
 size_t bwd_ws_bytes(const dfa_attn_desc& d)
 {
     const size_t rows = (size_t)d.B * d.Hq * (size_t)d.N;
-    return kStatusBytes + align256(rows * d.d * 4) + 2 * align256(rows * kAugRowBytes);
+    const size_t kv = (size_t)d.B * d.Hkv * (size_t)d.N * d.d * 4;
+    return kStatusBytes + align256(rows * d.d * 4) + 2 * align256(rows * kAugRowBytes) +
+           (bwd_blocked(d.N) ? 2 * align256(kv) : 0);
 }
 
 }  // namespace
@@ -599,13 +620,31 @@ dfa_status dfa_attn_bwd(const dfa_attn_desc* desc, const void* q, const void* k,
                                           aug_lse, aug_delta, dq_acc, sms, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward preprocess launch");
-    s = run_bwd_main(*desc, whole_layout(*desc), q, k, v, dout, aug_lse, aug_delta, dq_acc, dk,
-                     dv, 0, ws, st);
+    const bool blocked = bwd_blocked(desc->N);
+    const int64_t kv_elems = (int64_t)desc->B * desc->Hkv * desc->N * desc->d;
+    float* dk_acc = nullptr;
+    float* dv_acc = nullptr;
+    if (blocked) {
+        dk_acc = reinterpret_cast<float*>(aug_delta + align256((size_t)rows * kAugRowBytes));
+        dv_acc = reinterpret_cast<float*>((char*)dk_acc + align256((size_t)kv_elems * 4));
+        e = cudaMemsetAsync(dk_acc, 0, (size_t)kv_elems * 4, st);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(dv_acc, 0, (size_t)kv_elems * 4, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "dK/dV accumulator clear");
+    }
+    s = run_bwd_main(*desc, whole_layout(*desc), q, k, v, dout, aug_lse, aug_delta, dq_acc,
+                     blocked ? (void*)dk_acc : dk, blocked ? (void*)dv_acc : dv, blocked ? 1 : 0,
+                     ws, st);
     if (s != DFA_OK)
         return s;
     e = launch_f32_to_bf16(rows * desc->d, dq_acc, dq, sms, st);
+    if (e == cudaSuccess && blocked)
+        e = launch_f32_to_bf16(kv_elems, dk_acc, dk, sms, st);
+    if (e == cudaSuccess && blocked)
+        e = launch_f32_to_bf16(kv_elems, dv_acc, dv, sms, st);
     if (e != cudaSuccess)
-        return cuda_fail(e, "dQ conversion launch");
+        return cuda_fail(e, "dQ/dK/dV conversion launch");
     return DFA_OK;
 }
 

@@ -107,6 +107,21 @@ struct QRange {
     int32_t p, i0, i1, if0, if1;
 };
 
+// Query blocking: a unit covers only the query tiles of its block (the same
+// local tile range of every query chunk), so that the units running at one
+// time share a bounded set of Q / dO / dQ rows in L2.
+__device__ __forceinline__ QRange clamp_block(const BwdParams& pr, const Unit& un, QRange r)
+{
+    if (pr.nqblk > 1) {
+        const int32_t b0 = un.qblk * pr.qblk_tiles, b1 = b0 + pr.qblk_tiles;
+        r.i0 = max(r.i0, b0);
+        r.i1 = min(r.i1, b1);
+    }
+    if (r.i1 < r.i0)
+        r.i1 = r.i0;
+    return r;
+}
+
 __device__ __forceinline__ QRange q_range(const BwdParams& pr, const Unit& un, int s)
 {
     QRange r;
@@ -117,7 +132,7 @@ __device__ __forceinline__ QRange q_range(const BwdParams& pr, const Unit& un, i
         r.i1 = nqt;
         r.if0 = 0;
         r.if1 = pr.chunk_q / BQ;
-        return r;
+        return clamp_block(pr, un, r);
     }
     const DevMap& km = pr.kmap[un.chunk];
     const DevMap& qm = pr.qmap[r.p];
@@ -132,11 +147,21 @@ __device__ __forceinline__ QRange q_range(const BwdParams& pr, const Unit& un, i
     const int32_t end_full = lo_max <= pk_min ? map_count_le(qm, hi_min - 1) : 0;
     r.i0 = first_vis / BQ;
     r.i1 = ceil_div(end_vis, BQ);
-    if (r.i1 < r.i0)
-        r.i1 = r.i0;
     r.if0 = ceil_div(first_full, BQ);
     r.if1 = end_full / BQ;
-    return r;
+    return clamp_block(pr, un, r);
+}
+
+// Unit u: slices (b, kv head) outermost, then query blocks, then the key
+// units of the slice in the table's order.
+__device__ __forceinline__ Unit bwd_unit(const BwdParams& p, int u)
+{
+    const int ups = p.units.units_per_slice;
+    const int per = p.nqblk * ups;
+    const int slice = u / per, r = u - slice * per;
+    Unit un = decode_unit(p.units, p.BHkv, kKvRows, slice * ups + r % ups, true);
+    un.qblk = r / ups;
+    return un;
 }
 
 __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& un)
@@ -183,7 +208,7 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
     }
     uint32_t uc = 0, qc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        Unit un = bwd_unit(p, u);
         if (unit_steps(p, un) == 0)
             continue;
         const int b = un.slice / p.Hkv, hk = un.slice % p.Hkv;
@@ -279,7 +304,7 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
     const uint64_t dDA = sdesc_sw32(smem_u32(sh.smem + C::kDA0), 256);
     uint32_t uc = 0, m = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        Unit un = bwd_unit(p, u);
         const int T = unit_steps(p, un);
         if (T == 0)
             continue;
@@ -332,7 +357,7 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
     const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs0), 16384, 1024);
     uint32_t uc = 0, n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        Unit un = bwd_unit(p, u);
         const int T = unit_steps(p, un);
         if (T == 0)
             continue;
@@ -394,7 +419,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        Unit un = bwd_unit(p, u);
         const int T = unit_steps(p, un);
         const bool kvalid = r < un.nvalid;
         const int32_t pk = kvalid ? map_pos(p.kmap[un.chunk], un.row0 + r) : 0;
@@ -509,9 +534,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                 for (int e = 0; e < 32; ++e)
                     o[e] = 0u;
             }
-            if (!kvalid)
-                continue;
-            if (p.dkv_mode == 0) {
+            if (kvalid && p.dkv_mode == 0) {
                 uint4* dst =
                     reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(outp) + orow * D + c0);
 #pragma unroll
@@ -524,20 +547,38 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                                     __uint_as_float(o[8 * e + 5]) * mul),
                                         pack_bf16x2(__uint_as_float(o[8 * e + 6]) * mul,
                                                     __uint_as_float(o[8 * e + 7]) * mul));
-            } else {
-                float4* dst =
-                    reinterpret_cast<float4*>(reinterpret_cast<float*>(outp) + orow * D + c0);
+            }
+            if (p.dkv_mode != 0 && T > 0) {
+                // fp32 accumulators shared with other units of this key tile
+                // (other query blocks, other chunk-pair calls): atomic adds,
+                // made row-contiguous through one dS^T tile per warpgroup (free
+                // once the unit's products are complete): each thread stores
+                // its row's 32 values (16-byte pieces XOR-swizzled by row),
+                // then each warp adds whole rows, 128 bytes per instruction
+                float* stage = reinterpret_cast<float*>(sh.smem + C::kDs0 + h * C::kDsBytes);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float4 v = dst[e];
-                    v.x += __uint_as_float(o[4 * e + 0]) * mul;
-                    v.y += __uint_as_float(o[4 * e + 1]) * mul;
-                    v.z += __uint_as_float(o[4 * e + 2]) * mul;
-                    v.w += __uint_as_float(o[4 * e + 3]) * mul;
-                    dst[e] = v;
+                for (int e = 0; e < 8; ++e)
+                    *reinterpret_cast<float4*>(stage + r * 32 + ((e ^ (r & 7)) * 4)) =
+                        make_float4(__uint_as_float(o[4 * e + 0]) * mul,
+                                    __uint_as_float(o[4 * e + 1]) * mul,
+                                    __uint_as_float(o[4 * e + 2]) * mul,
+                                    __uint_as_float(o[4 * e + 3]) * mul);
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
+                const int wq = warp & 3;
+                const size_t rbase = (size_t)un.slice * p.Lk + (size_t)un.chunk * p.chunk_k + un.row0;
+                for (int rr = wq * 32; rr < wq * 32 + 32; ++rr) {
+                    if (rr >= un.nvalid)
+                        break;
+                    const float val = stage[rr * 32 + (((lane >> 2) ^ (rr & 7)) * 4) + (lane & 3)];
+                    atomicAdd(reinterpret_cast<float*>(outp) + (rbase + rr) * D + c0 + lane, val);
                 }
+                asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
             }
         }
+        // both warpgroups staged through the shared dS^T tiles: neither may
+        // write the next unit's dS^T before the other has finished
+        if (p.dkv_mode != 0 && T > 0)
+            asm volatile("bar.sync 3, 256;" ::: "memory");
         tc_fence_before();
     }
 }
@@ -556,7 +597,7 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
     const float sc = p.scale;
     uint32_t n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-        Unit un = decode_unit(p.units, p.BHkv, kKvRows, u, true);
+        Unit un = bwd_unit(p, u);
         if (unit_steps(p, un) == 0)
             continue;
         const int b0 = un.slice / p.Hkv, hk = un.slice % p.Hkv;

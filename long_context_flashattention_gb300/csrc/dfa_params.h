@@ -114,6 +114,7 @@ struct Unit {
     int32_t chunk;   // chunk index
     int32_t row0;    // first local row of the unit inside the chunk
     int32_t nvalid;  // rows of the unit inside the segment (<= rows_per_unit)
+    int32_t qblk;    // backward: query block of the unit (0 without blocking)
 };
 
 DFA_HD Unit decode_unit(const UnitTable& t, int32_t nslices, int32_t rows_per_unit, int32_t u,
@@ -142,6 +143,7 @@ DFA_HD Unit decode_unit(const UnitTable& t, int32_t nslices, int32_t rows_per_un
     r.row0 = t.seg_start[seg] + k * rows_per_unit;
     int32_t rem = t.seg_start[seg] + t.seg_len[seg] - r.row0;
     r.nvalid = rem < rows_per_unit ? rem : rows_per_unit;
+    r.qblk = 0;
     return r;
 }
 
@@ -212,7 +214,9 @@ struct BwdParams {
     int32_t causal;
     float scale, scale_log2;
     int32_t total_units;
-    int32_t dkv_mode;            // 0: write bf16 dK/dV; 1: accumulate into fp32
+    int32_t dkv_mode;            // 0: write bf16 dK/dV; 1: add into fp32 (atomic)
+    int32_t nqblk;               // query blocks per key tile (1: no blocking)
+    int32_t qblk_tiles;          // query tiles per block and chunk
     int32_t ndocs;               // packed documents (0: none)
     const int64_t* docs;         // [ndocs + 1] cumulative positions (device)
     UnitTable units;

@@ -33,8 +33,9 @@ def test_status_strings(L):
 def test_workspace_sizes():
     d = dfa.make_desc(1, 32, 32, 131072, 128, P=8, partition="striped")
     assert dfa.workspace_size(d, dfa.OP_FWD) == 256
-    # status word, fp32 dQ accumulator, 32-byte -LSE/scale and -D records per row
-    need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32
+    # status word, fp32 dQ accumulator, 32-byte -LSE/scale and -D records per row,
+    # and (query blocking above 64K rows per head) fp32 dK and dV
+    need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32 + 2 * 32 * 131072 * 128 * 4
     assert dfa.workspace_size(d, dfa.OP_BWD) == need
     assert dfa.workspace_size(d, dfa.OP_CHUNK_BWD) == 256 + 2 * 32 * 131072 * 32
     bad = dfa.make_desc(1, 32, 32, 1000, 128, P=3)
