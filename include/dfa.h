@@ -247,6 +247,46 @@ dfa_status dfa_ring_fwd(const dfa_attn_desc* desc, const dfa_ring_worker* worker
                         void* copy_stream);
 
 /*
+ * dfa_attn_step_host -- one training step of attention with its tensors in
+ * HOST memory, in natural token order: the permute into desc's worker-major
+ * order, dfa_attn_fwd, dfa_attn_bwd and the permutes back (the forward and
+ * recomputation backward of the FlashAttention glossary entry over the
+ * partition of desc), with the host-to-device and device-to-host copies
+ * inside the call.  The pages describe no counterpart: this is the
+ * library's host-streaming executor.
+ *
+ * The work is cut into groups of kv_heads_per_group key/value heads of one
+ * batch item, each with its Hq/Hkv query heads (heads never interact, so a
+ * group is a complete problem of B = 1).  Group g's upload (h2d_stream), its
+ * compute (compute_stream) and its download (d2h_stream) are ordered by
+ * events, so that group g+1 uploads and group g-1 downloads while group g
+ * computes; device staging is double-buffered in ws.  With pinned host
+ * memory the copies overlap the compute; pageable memory gives the same
+ * results with the copies serialised by the driver.  h2d_stream or
+ * d2h_stream NULL: those copies run on compute_stream, in order.
+ *   h_q, h_dout [B,Hq,N,d] bf16; h_k, h_v [B,Hkv,N,d] bf16 (read);
+ *   h_o, h_dq [B,Hq,N,d] bf16, h_lse [B,Hq,N] fp32, h_dk, h_dv [B,Hkv,N,d]
+ *   bf16 (written; O is the forward output, LSE its natural-log row
+ *   log-sum-exp).  Host buffers must stay valid and untouched until
+ *   compute_stream has passed the call's work.
+ *   kv_heads_per_group: a divisor of Hkv, or 0 for the library's choice
+ *   (at least 8 groups where B*Hkv allows).
+ *   ws: dfa_attn_step_host_workspace_size(desc, kv_heads_per_group) bytes,
+ *   status word first (dfa_stream_status reads the backward's timeouts).
+ * desc->o_fp32 must be 0 (DFA_ERR_UNSUPPORTED otherwise).  When the call
+ * returns, all of its work, on every stream, is ordered before later work
+ * on compute_stream; an error returned after work was queued still orders
+ * the queued work so.
+ */
+size_t dfa_attn_step_host_workspace_size(const dfa_attn_desc* desc,
+                                         int32_t kv_heads_per_group);
+dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* h_q, const void* h_k,
+                              const void* h_v, const void* h_dout, void* h_o, float* h_lse,
+                              void* h_dq, void* h_dk, void* h_dv, int32_t kv_heads_per_group,
+                              void* ws, size_t ws_bytes, void* compute_stream,
+                              void* h2d_stream, void* d2h_stream);
+
+/*
  * dfa_decode -- split-KV decoding: T query tokens per sequence against L
  * cached keys (FlashAttention glossary entry, the Flash-Decoding variant:
  * the keys are cut into splits of split_len, each split gives a normalised

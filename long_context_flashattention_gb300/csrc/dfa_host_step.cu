@@ -1,0 +1,364 @@
+// dfa_host_step.cu -- the host-streaming executor: one attention training
+// step (permute, forward, recomputation backward, permute back) whose tensors
+// live in host memory, cut into groups of whole key/value heads so that the
+// copies of neighbouring groups overlap a group's compute.
+//
+// Host code only.  Per group g (slot s = g % 2 of the double-buffered
+// staging):
+//   h2d stream:      [wait in_free[s]]  upload q, k, v, dO of g  -> up[s]
+//   compute stream:  wait up[s]; permute in -> in_free[s]; [wait down[s]]
+//                    forward; backward; permute out into out staging[s]
+//                    -> done
+//   d2h stream:      wait done; download o, lse, dq, dk, dv of g -> down[s]
+// in_free[s] lets the upload of g+2 reuse the input slot once g's inputs are
+// consumed; down[s] keeps the compute of g+2 from overwriting the output
+// slot before g's download has read it.  When the partition's storage order
+// is natural order (P = 1, contiguous, or stripes as long as a chunk) the
+// permutes are skipped: the compute reads the input slot and writes the
+// output slot directly, and in_free[s] is recorded after the backward.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dfa.h"
+
+namespace dfa {
+dfa_status set_error(dfa_status s, const char* fmt, ...);
+}
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Groups of at least this many when B*Hkv allows: the first upload and the
+// last download, which nothing hides, are then an eighth of the copies.
+constexpr int kMinGroups = 8;
+
+int auto_group(const dfa_attn_desc& d)
+{
+    int best = 1;
+    for (int g = 1; g <= d.Hkv; ++g)
+        if (d.Hkv % g == 0 && (int64_t)d.B * (d.Hkv / g) >= kMinGroups)
+            best = g;
+    return best;
+}
+
+dfa_attn_desc group_desc(const dfa_attn_desc& d, int gk)
+{
+    dfa_attn_desc g = d;
+    g.B = 1;
+    g.Hkv = gk;
+    g.Hq = gk * (d.Hq / d.Hkv);
+    return g;
+}
+
+// Natural order is the storage order: every worker's rows are one run of
+// positions starting at p n.
+bool identity_order(const dfa_attn_desc& d)
+{
+    const int64_t n = d.N / d.P;
+    for (int p = 0; p < d.P; ++p) {
+        dfa_pos_map m;
+        if (dfa_partition_map(&d, p, &m) != DFA_OK)
+            return false;
+        if (m.nseg != 1 || m.base[0] != (int64_t)p * n ||
+            !(m.len[0] <= m.blk || m.blk_stride == m.blk))
+            return false;
+    }
+    return true;
+}
+
+// Byte sizes of one group's tensors and the workspace layout built on them.
+struct Plan {
+    int gk = 0, groups = 0;
+    bool ident = false;
+    dfa_attn_desc gd{};
+    size_t qb = 0, kb = 0, lb = 0;      // one group's q (= o, dq, dO), k (= v, dk, dv), lse
+    size_t bwd_ws = 0;                   // the group backward's workspace (status word first)
+    size_t in_set = 0, out_set = 0;      // one input set (q k v dO), one output set
+    size_t off_in[2] = {0, 0}, off_out[2] = {0, 0}, off_pin = 0, off_pout = 0, total = 0;
+};
+
+dfa_status make_plan(const dfa_attn_desc* desc, int32_t kv_heads_per_group, Plan& pl)
+{
+    if (dfa_workspace_size(desc, DFA_OP_BWD) == 0)  // validates desc, sets the error text
+        return DFA_ERR_INVALID_ARG;
+    if (desc->o_fp32 != 0)
+        return dfa::set_error(DFA_ERR_UNSUPPORTED, "dfa_attn_step_host: O is bf16 here "
+                              "(desc->o_fp32 must be 0)");
+    if (kv_heads_per_group < 0 || (kv_heads_per_group > 0 && desc->Hkv % kv_heads_per_group))
+        return dfa::set_error(DFA_ERR_INVALID_ARG, "dfa_attn_step_host: kv_heads_per_group "
+                              "(%d) must be 0 or divide Hkv (%d)", kv_heads_per_group,
+                              desc->Hkv);
+    pl.gk = kv_heads_per_group ? kv_heads_per_group : auto_group(*desc);
+    pl.groups = desc->B * (desc->Hkv / pl.gk);
+    pl.gd = group_desc(*desc, pl.gk);
+    pl.ident = identity_order(*desc);
+    const size_t rows_q = (size_t)pl.gd.Hq * desc->N, rows_k = (size_t)pl.gk * desc->N;
+    pl.qb = rows_q * desc->d * 2;
+    pl.kb = rows_k * desc->d * 2;
+    pl.lb = rows_q * 4;
+    pl.bwd_ws = dfa_workspace_size(&pl.gd, DFA_OP_BWD);
+    if (pl.bwd_ws == 0)
+        return DFA_ERR_INVALID_ARG;
+    pl.in_set = 2 * align256(pl.qb) + 2 * align256(pl.kb);
+    pl.out_set = 2 * align256(pl.qb) + align256(pl.lb) + 2 * align256(pl.kb);
+    size_t off = align256(pl.bwd_ws);
+    for (int s = 0; s < 2; ++s) {
+        pl.off_in[s] = off;
+        off += pl.in_set;
+    }
+    for (int s = 0; s < 2; ++s) {
+        pl.off_out[s] = off;
+        off += pl.out_set;
+    }
+    pl.off_pin = pl.off_pout = off;
+    if (!pl.ident) {  // the worker-major copies the kernels read and write
+        pl.off_pin = off;
+        off += pl.in_set;
+        pl.off_pout = off;
+        off += pl.out_set;
+    }
+    pl.total = off;
+    return DFA_OK;
+}
+
+// The five tensors of an input set (q, k, v, dO) or output set (o, lse, dq,
+// dk, dv) at base.
+struct InSet {
+    char *q, *k, *v, *dout;
+};
+struct OutSet {
+    char *o, *lse, *dq, *dk, *dv;
+};
+
+InSet in_set(char* base, const Plan& pl)
+{
+    InSet s;
+    s.q = base;
+    s.k = s.q + align256(pl.qb);
+    s.v = s.k + align256(pl.kb);
+    s.dout = s.v + align256(pl.kb);
+    return s;
+}
+
+OutSet out_set(char* base, const Plan& pl)
+{
+    OutSet s;
+    s.o = base;
+    s.lse = s.o + align256(pl.qb);
+    s.dq = s.lse + align256(pl.lb);
+    s.dk = s.dq + align256(pl.qb);
+    s.dv = s.dk + align256(pl.kb);
+    return s;
+}
+
+struct Events {
+    enum { kEntry, kUp0, kUp1, kInFree0, kInFree1, kDone, kDown0, kDown1, kTailUp, kCount };
+    cudaEvent_t e[kCount] = {};
+    ~Events()
+    {
+        for (cudaEvent_t x : e)
+            if (x)
+                cudaEventDestroy(x);
+    }
+    cudaError_t create()
+    {
+        for (cudaEvent_t& x : e) {
+            cudaError_t r = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+            if (r != cudaSuccess)
+                return r;
+        }
+        return cudaSuccess;
+    }
+};
+
+dfa_status cuda_err(cudaError_t e, const char* what)
+{
+    return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_step_host: %s: %s", what,
+                          cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" size_t dfa_attn_step_host_workspace_size(const dfa_attn_desc* desc,
+                                                    int32_t kv_heads_per_group)
+{
+    Plan pl;
+    return make_plan(desc, kv_heads_per_group, pl) == DFA_OK ? pl.total : 0;
+}
+
+extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* h_q,
+                                         const void* h_k, const void* h_v, const void* h_dout,
+                                         void* h_o, float* h_lse, void* h_dq, void* h_dk,
+                                         void* h_dv, int32_t kv_heads_per_group, void* ws,
+                                         size_t ws_bytes, void* compute_stream,
+                                         void* h2d_stream, void* d2h_stream)
+{
+    Plan pl;
+    dfa_status st = make_plan(desc, kv_heads_per_group, pl);
+    if (st != DFA_OK)
+        return st;
+    if (!h_q || !h_k || !h_v || !h_dout || !h_o || !h_lse || !h_dq || !h_dk || !h_dv)
+        return dfa::set_error(DFA_ERR_INVALID_ARG, "dfa_attn_step_host: a host pointer is NULL");
+    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < pl.total)
+        return dfa::set_error(DFA_ERR_WORKSPACE, "dfa_attn_step_host: workspace must be "
+                              "256-byte aligned and hold %zu bytes", pl.total);
+    const cudaStream_t cs = (cudaStream_t)compute_stream;
+    const cudaStream_t up = h2d_stream ? (cudaStream_t)h2d_stream : cs;
+    const cudaStream_t dn = d2h_stream ? (cudaStream_t)d2h_stream : cs;
+    Events ev;
+    cudaError_t e = ev.create();
+    if (e != cudaSuccess)
+        return cuda_err(e, "event creation");
+    // the staging slots may still be read by earlier work on compute_stream
+    e = cudaEventRecord(ev.e[Events::kEntry], cs);
+    if (e == cudaSuccess && up != cs)
+        e = cudaStreamWaitEvent(up, ev.e[Events::kEntry], 0);
+    if (e == cudaSuccess && dn != cs)
+        e = cudaStreamWaitEvent(dn, ev.e[Events::kEntry], 0);
+    if (e != cudaSuccess)
+        return cuda_err(e, "entry ordering");
+
+    char* base = (char*)ws;
+    const int per_b = desc->Hkv / pl.gk;
+    const int r = desc->Hq / desc->Hkv;
+    const int64_t heads_q = pl.gd.Hq, heads_k = pl.gk;
+    const int64_t d = desc->d;
+    auto host_off_q = [&](int g) {  // element offset of group g in a [B,Hq,N,d] tensor
+        return ((int64_t)(g / per_b) * desc->Hq + (int64_t)(g % per_b) * pl.gk * r) * desc->N;
+    };
+    auto host_off_k = [&](int g) {
+        return ((int64_t)(g / per_b) * desc->Hkv + (int64_t)(g % per_b) * pl.gk) * desc->N;
+    };
+    auto upload = [&](int g) -> cudaError_t {
+        const int s = g % 2;
+        const InSet in = in_set(base + pl.off_in[s], pl);
+        const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
+        cudaError_t x = cudaSuccess;
+        if (g >= 2)
+            x = cudaStreamWaitEvent(up, ev.e[Events::kInFree0 + s], 0);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync(in.q, (const char*)h_q + oq, pl.qb, cudaMemcpyHostToDevice, up);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync(in.k, (const char*)h_k + ok, pl.kb, cudaMemcpyHostToDevice, up);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync(in.v, (const char*)h_v + ok, pl.kb, cudaMemcpyHostToDevice, up);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync(in.dout, (const char*)h_dout + oq, pl.qb, cudaMemcpyHostToDevice,
+                                up);
+        if (x == cudaSuccess)
+            x = cudaEventRecord(ev.e[Events::kUp0 + s], up);
+        return x;
+    };
+    auto download = [&](int g) -> cudaError_t {
+        const int s = g % 2;
+        const OutSet out = out_set(base + pl.off_out[s], pl);
+        const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
+        const int64_t ol = host_off_q(g) * 4;
+        cudaError_t x = cudaStreamWaitEvent(dn, ev.e[Events::kDone], 0);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync((char*)h_o + oq, out.o, pl.qb, cudaMemcpyDeviceToHost, dn);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync((char*)h_lse + ol, out.lse, pl.lb, cudaMemcpyDeviceToHost, dn);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync((char*)h_dq + oq, out.dq, pl.qb, cudaMemcpyDeviceToHost, dn);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync((char*)h_dk + ok, out.dk, pl.kb, cudaMemcpyDeviceToHost, dn);
+        if (x == cudaSuccess)
+            x = cudaMemcpyAsync((char*)h_dv + ok, out.dv, pl.kb, cudaMemcpyDeviceToHost, dn);
+        if (x == cudaSuccess)
+            x = cudaEventRecord(ev.e[Events::kDown0 + s], dn);
+        return x;
+    };
+    auto compute = [&](int g) -> dfa_status {
+        const int s = g % 2;
+        const InSet in = in_set(base + pl.off_in[s], pl);
+        const OutSet out = out_set(base + pl.off_out[s], pl);
+        const InSet pin = pl.ident ? in : in_set(base + pl.off_pin, pl);
+        const OutSet pout = pl.ident ? out : out_set(base + pl.off_pout, pl);
+        const dfa_attn_desc* gd = &pl.gd;
+        cudaError_t x = cudaStreamWaitEvent(cs, ev.e[Events::kUp0 + s], 0);
+        if (x != cudaSuccess)
+            return cuda_err(x, "stream wait");
+        dfa_status t = DFA_OK;
+        if (!pl.ident) {
+            t = dfa_permute(gd, 0, in.q, pin.q, 2, d, heads_q, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 0, in.k, pin.k, 2, d, heads_k, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 0, in.v, pin.v, 2, d, heads_k, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 0, in.dout, pin.dout, 2, d, heads_q, cs);
+            if (t != DFA_OK)
+                return t;
+            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
+                return cuda_err(x, "event record");
+        }
+        // the output slot was last read by the download of group g - 2
+        if (pl.ident && g >= 2 && dn != cs &&
+            (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
+            return cuda_err(x, "stream wait");
+        t = dfa_attn_fwd(gd, pin.q, pin.k, pin.v, pout.o, (float*)pout.lse, ws, 256, cs);
+        if (t == DFA_OK)
+            t = dfa_attn_bwd(gd, pin.q, pin.k, pin.v, pout.o, pin.dout, (const float*)pout.lse,
+                             pout.dq, pout.dk, pout.dv, ws, pl.bwd_ws, cs);
+        if (t != DFA_OK)
+            return t;
+        if (pl.ident) {
+            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
+                return cuda_err(x, "event record");
+        } else {
+            if (g >= 2 && dn != cs &&
+                (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
+                return cuda_err(x, "stream wait");
+            t = dfa_permute(gd, 1, pout.o, out.o, 2, d, heads_q, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 1, pout.lse, out.lse, 4, 1, heads_q, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 1, pout.dq, out.dq, 2, d, heads_q, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 1, pout.dk, out.dk, 2, d, heads_k, cs);
+            if (t == DFA_OK)
+                t = dfa_permute(gd, 1, pout.dv, out.dv, 2, d, heads_k, cs);
+            if (t != DFA_OK)
+                return t;
+        }
+        if ((x = cudaEventRecord(ev.e[Events::kDone], cs)) != cudaSuccess)
+            return cuda_err(x, "event record");
+        return DFA_OK;
+    };
+
+    // Issue order: the next group's upload goes into its queue before this
+    // group's compute, so the copy engine never waits on the host.
+    e = upload(0);
+    if (e != cudaSuccess)
+        st = cuda_err(e, "upload");
+    for (int g = 0; g < pl.groups && st == DFA_OK; ++g) {
+        if (g + 1 < pl.groups && (e = upload(g + 1)) != cudaSuccess) {
+            st = cuda_err(e, "upload");
+            break;
+        }
+        if ((st = compute(g)) != DFA_OK)
+            break;
+        if ((e = download(g)) != cudaSuccess)
+            st = cuda_err(e, "download");
+    }
+    // Join: everything queued on the copy streams is ordered before later
+    // work on compute_stream, on success and on error alike.
+    cudaError_t j = cudaSuccess;
+    if (up != cs) {
+        j = cudaEventRecord(ev.e[Events::kTailUp], up);
+        if (j == cudaSuccess)
+            j = cudaStreamWaitEvent(cs, ev.e[Events::kTailUp], 0);
+    }
+    if (j == cudaSuccess && dn != cs) {
+        j = cudaEventRecord(ev.e[Events::kDone], dn);
+        if (j == cudaSuccess)
+            j = cudaStreamWaitEvent(cs, ev.e[Events::kDone], 0);
+    }
+    if (st == DFA_OK && j != cudaSuccess)
+        st = cuda_err(j, "join");
+    return st;
+}

@@ -87,6 +87,9 @@ def lib():
             "dfa_permute": (i32, [D, i32, vp, vp, i32, i64, i64, vp]),
             "dfa_permute_rope": (i32, [D, i32, vp, vp, i64, ctypes.c_float, vp]),
             "dfa_ring_fwd": (i32, [D, ctypes.POINTER(RingWorker), vp, sz, i32, vp, vp]),
+            "dfa_attn_step_host_workspace_size": (sz, [D, i32]),
+            "dfa_attn_step_host": (i32, [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp,
+                                         vp, vp]),
             "dfa_decode_workspace_size": (sz, [D, i32, i64, i32]),
             "dfa_decode": (i32, [D, i32, i64, i64, vp, vp, vp, vp, vp, i32, vp, sz, vp]),
             "dfa_make_schedule": (i32, [D, i32, i32, ctypes.POINTER(Schedule)]),
@@ -388,6 +391,57 @@ def ring_fwd(q_chunks, k_chunks, v_chunks, partition, stripe=1, causal=True, sca
                                                             outs)])
     _check(lib().dfa_ring_fwd(ctypes.byref(desc), arr, _ptr(ws), ws.numel(), int(overlap),
                               _stream(stream), _stream(copy_stream) if overlap else None))
+    return outs
+
+
+_up_streams, _down_streams = {}, {}
+
+
+def step_host_workspace(desc: AttnDesc, kv_heads_per_group=0, device=None) -> torch.Tensor:
+    n = int(lib().dfa_attn_step_host_workspace_size(ctypes.byref(desc), kv_heads_per_group))
+    if n == 0:
+        raise DfaError(1, "invalid arguments for workspace sizing: " +
+                       lib().dfa_last_error().decode())
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def attn_step_host(q, k, v, dout, causal=True, scale=None, P=1, partition="contiguous",
+                   stripe=1, docs=None, kv_heads_per_group=0, outs=None, ws=None, overlap=True,
+                   stream=None, h2d_stream=None, d2h_stream=None):
+    """One attention training step from host memory (dfa_attn_step_host): q/dout
+    [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 CPU tensors in natural order (pinned for
+    the copies to overlap the compute).  Returns CPU tensors (o, lse, dq, dk,
+    dv), pinned when allocated here; they hold the results once the compute
+    stream has passed the call (e.g. after torch.cuda.synchronize()).  With
+    overlap the uploads and downloads run on two extra streams (given, or kept
+    per device)."""
+    for t in (q, k, v, dout):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v, dout must be contiguous bf16 host tensors")
+    desc = desc_for(q, k, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe,
+                    docs=docs)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if outs is None:
+        def pinned(*shape, dtype=torch.bfloat16):
+            return torch.empty(*shape, dtype=dtype, pin_memory=True)
+        outs = (pinned(B, Hq, N, d), pinned(B, Hq, N, dtype=torch.float32), pinned(B, Hq, N, d),
+                pinned(B, Hkv, N, d), pinned(B, Hkv, N, d))
+    for t in outs:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("outputs must be contiguous host tensors")
+    if ws is None:
+        ws = step_host_workspace(desc, kv_heads_per_group, dev)
+    if overlap:
+        h2d_stream = h2d_stream or _up_streams.setdefault(dev, torch.cuda.Stream(dev))
+        d2h_stream = d2h_stream or _down_streams.setdefault(dev, torch.cuda.Stream(dev))
+    o, lse, dq, dk, dv = outs
+    _check(lib().dfa_attn_step_host(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                    _ptr(o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                                    kv_heads_per_group, _ptr(ws), ws.numel(), _stream(stream),
+                                    _stream(h2d_stream) if overlap else None,
+                                    _stream(d2h_stream) if overlap else None))
     return outs
 
 

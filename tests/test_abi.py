@@ -143,3 +143,54 @@ def test_schedule_eta_closed_forms():
     n = N // P
     s = dfa.make_schedule(N, P, "striped")
     assert abs(s["eta_flops"] - (N * (N + 1) / 2) / (P * P * n * (n + 1) / 2)) < 1e-12
+
+
+def _step_host_ws(desc, gk):
+    return int(dfa.lib().dfa_attn_step_host_workspace_size(ctypes.byref(desc), gk))
+
+
+def test_step_host_workspace_layout():
+    """Group backward workspace, two input and two output staging slots, and
+    (when the partition's storage order is not natural order) one worker-major
+    input and output set."""
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    B, Hq, Hkv, N, d = 1, 32, 32, 131072, 128
+    for kind, P, extra in (("contiguous", 8, 0), ("striped", 8, 1), ("balanced", 8, 1),
+                           ("striped", 1, 0)):
+        desc = dfa.make_desc(B, Hq, Hkv, N, d, P=P, partition=kind)
+        gk = 4                                    # 8 groups of 4 key/value heads
+        gdesc = dfa.make_desc(1, gk, gk, N, d, P=P, partition=kind)
+        qb, kb, lb = gk * N * d * 2, gk * N * d * 2, gk * N * 4
+        in_set, out_set = 2 * a256(qb) + 2 * a256(kb), 2 * a256(qb) + a256(lb) + 2 * a256(kb)
+        need = (a256(dfa.workspace_size(gdesc, dfa.OP_BWD)) + 2 * in_set + 2 * out_set +
+                extra * (in_set + out_set))
+        assert _step_host_ws(desc, gk) == need
+        assert _step_host_ws(desc, 0) == need     # the automatic choice
+    # a token stripe as long as a chunk keeps natural order
+    d1 = dfa.make_desc(1, 4, 4, 4096, 64, P=4, partition="striped", stripe=1024)
+    d2 = dfa.make_desc(1, 4, 4, 4096, 64, P=4, partition="contiguous")
+    assert _step_host_ws(d1, 1) == _step_host_ws(d2, 1)
+    # fewer than 8 key/value heads in all: one head per group
+    small = dfa.make_desc(2, 4, 2, 1024, 128)
+    assert _step_host_ws(small, 0) == _step_host_ws(small, 1)
+
+
+def test_step_host_validation(L):
+    desc = dfa.make_desc(1, 4, 2, 256, 64)
+    assert _step_host_ws(desc, 3) == 0                      # does not divide Hkv
+    assert _step_host_ws(desc, -1) == 0
+    assert _step_host_ws(dfa.make_desc(1, 4, 2, 256, 64, o_fp32=True), 0) == 0
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.c_void_p((ctypes.addressof(buf) + 255) & ~255)
+    args = [p] * 9
+    assert L.dfa_attn_step_host(ctypes.byref(desc), *args, 3, p, 1 << 40, None, None,
+                                None) == 1
+    assert L.dfa_attn_step_host(ctypes.byref(desc), None, *args[1:], 0, p, 1 << 40, None, None,
+                                None) == 1
+    assert L.dfa_attn_step_host(ctypes.byref(desc), *args, 0, p, 16, None, None, None) == 3
+    assert b"workspace" in L.dfa_last_error()
+    fp32 = dfa.make_desc(1, 4, 2, 256, 64, o_fp32=True)
+    assert L.dfa_attn_step_host(ctypes.byref(fp32), *args, 0, p, 1 << 40, None, None,
+                                None) == 2
