@@ -35,7 +35,6 @@ import torch  # noqa: E402
 
 METRIC = "causal attn fwd+bwd TFLOPS (bf16, 1 GB300) and % of dense BF16 tensor peak"
 WORKLOAD = "llama7b_128k"
-PARTITION = "striped"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -162,7 +161,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
-    P, kind = w.P, PARTITION
+    P, kind = w.P, w.partitions[0]
     dfa.lib()
 
     # inputs, resident in HBM before timing (larger than L2: 1 GiB per tensor)
@@ -278,8 +277,10 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     d2h_ms = e0.elapsed_time(e1)
 
-    # standalone LSE merge at this workload's size (k = P partials per row)
-    rows = w.B * w.Hq * w.N
+    # standalone LSE merge at this workload's size (k = P partials per row;
+    # at most 4M rows, 17 GB of partials at k = 8, so that the largest
+    # workload's merge stays within memory beside its step buffers)
+    rows = min(w.B * w.Hq * w.N, 1 << 22)
     parts_o = torch.randn(P, rows, w.d, device=dev)
     parts_l = 4 * torch.randn(P, rows, device=dev)
     m_out = torch.empty(rows, w.d, dtype=torch.bfloat16, device=dev)
@@ -298,6 +299,39 @@ def run_gpu(args):
     merge_ms = m0.elapsed_time(m1) / reps
     merge_bytes = rows * (P * (4 * w.d + 4) + (2 * w.d + 4))
     del parts_o, parts_l
+
+    # the same merge at the grouped-query 64K workload's size: B2 Hq32 N65536
+    # rows (as many as here), k = 16 partials (P = 16)
+    rows16, k16 = 2 * 32 * 65536, 16
+    parts_o = torch.randn(k16, rows16, w.d, device=dev)
+    parts_l = 4 * torch.randn(k16, rows16, device=dev)
+    m_out = torch.empty(rows16, w.d, dtype=torch.bfloat16, device=dev)
+    m_lse = torch.empty(rows16, device=dev)
+    for _ in range(3):
+        dfa.lse_merge(parts_o, parts_l, out_fp32=False, o_out=m_out, lse_out=m_lse)
+    torch.cuda.synchronize(dev)
+    m0.record(stream)
+    for _ in range(reps):
+        dfa.lse_merge(parts_o, parts_l, out_fp32=False, o_out=m_out, lse_out=m_lse)
+    m1.record(stream)
+    torch.cuda.synchronize(dev)
+    merge16_ms = m0.elapsed_time(m1) / reps
+    merge16_bytes = rows16 * (k16 * (4 * w.d + 4) + (2 * w.d + 4))
+    del parts_o, parts_l, m_out, m_lse
+
+    # the plain permute of Q into worker-major order
+    p_out = torch.empty_like(qg)
+    for _ in range(3):
+        dfa.permute(qg, P, kind, out=p_out)
+    torch.cuda.synchronize(dev)
+    m0.record(stream)
+    for _ in range(reps):
+        dfa.permute(qg, P, kind, out=p_out)
+    m1.record(stream)
+    torch.cuda.synchronize(dev)
+    perm_ms = m0.elapsed_time(m1) / reps
+    perm_bytes = 2 * qg.numel() * qg.element_size()
+    del p_out
 
     # permute fused with the rotary embedding at global positions, on Q
     r_out = torch.empty_like(qg)
@@ -396,6 +430,18 @@ def run_gpu(args):
                   "bytes": merge_bytes, "ms": round(merge_ms, 4),
                   "achieved": round(merge_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                   "frac": round(merge_gbs / pk["hbm_gbs"], 4)},
+        "merge_k16": {"kernel": "dfa::lse_merge_kernel", "k": k16, "rows": rows16,
+                      "size": "grouped-query attention B2 Hq32 N65536 output rows, P = 16",
+                      "bytes": merge16_bytes, "ms": round(merge16_ms, 4),
+                      "achieved": round(merge16_bytes / (merge16_ms * 1e-3) / 1e9, 1),
+                      "peak": pk["hbm_gbs"], "unit": "GB/s",
+                      "frac": round(merge16_bytes / (merge16_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                    4)},
+        "permute": {"kernel": "dfa::permute_kernel", "tensor": "Q", "bytes": perm_bytes,
+                    "ms": round(perm_ms, 4),
+                    "achieved": round(perm_bytes / (perm_ms * 1e-3) / 1e9, 1),
+                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(perm_bytes / (perm_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
         "rope_permute": {"kernel": "dfa::permute_rope_kernel", "tensor": "Q",
                          "bytes": rope_bytes, "ms": round(rope_ms, 4),
                          "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
@@ -460,10 +506,23 @@ def cpu_baseline(q, k, v, do, w, budget_s=15.0):
         done += len(r)
         batch = min(batch * 2, 512)
     value = flops / t_used / 1e12
+    # the whole oracle (forward and every gradient) on the tiny workload, in full
+    from long_context_flashattention_gb300.inputs import WORKLOADS, make_workload
+    tw = WORKLOADS["tiny"]
+    tq, tk, tv, tdo = make_workload(tw)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(tq, tk, tv)
+    oracle.attn_bwd(tq, tk, tv, tdo)
+    tiny_s = time.perf_counter() - t0
     return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} seeded sampled query rows of {w.name}: fp64 forward row + dQ "
                       f"row each ({t_used:.1f} s)",
-            "seconds": round(t_used, 2)}
+            "seconds": round(t_used, 2),
+            "extrapolated_full_s": round((w.flops_fwd + w.flops_bwd) / (value * 1e12), 1),
+            "extrapolated_basis": "forward and backward FLOPs of the whole workload at the "
+                                  "sampled rows' rate (extrapolated, not run)",
+            "tiny_full_s": round(tiny_s, 4),
+            "tiny_full_tflops": round((tw.flops_fwd + tw.flops_bwd) / tiny_s / 1e12, 6)}
 
 
 def run_reference(args):
@@ -488,7 +547,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_total / args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name} causal, P={w.P} {PARTITION} partition",
+        "config": {"workload": f"{w.name} causal, P={w.P} {w.partitions[0]} partition",
                    "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"],
                          "kind": "oracle", "sample": cb["sample"]},
