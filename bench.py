@@ -201,7 +201,8 @@ def run_gpu(args):
     # permutes in, forward, backward (preprocess, main kernel, dQ conversion;
     # with query blocking above 64K rows per head also dK and dV conversions),
     # permutes out
-    launches_per_step = 4 + 1 + (5 if w.N > 65536 else 3) + 5
+    blocked = w.N > 65536
+    launches_per_step = 4 + 1 + (5 if blocked else 3) + 5
 
     def barrier():
         torch.cuda.synchronize(dev)

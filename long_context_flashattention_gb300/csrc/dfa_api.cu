@@ -303,7 +303,10 @@ dfa_status check_ws(void* ws, size_t have, size_t need)
 // blocks of about kBwdBlockRows rows (same local tile range in every query
 // chunk): the units running at one time then share one block's Q, dO and dQ
 // rows (about 32 MB) in L2 instead of a whole head's, and dK / dV are summed
-// over the blocks in fp32.
+// over the blocks in fp32.  The count is per head, not per key/value group:
+// measured on grouped-query attention (4 query heads per key/value head, 64K
+// rows), blocks of 8K rows per head ran the backward slower than no blocks,
+// the running units then streaming the group's rows in near lockstep.
 constexpr int64_t kBwdBlockAbove = 65536, kBwdBlockRows = 32768;
 
 bool bwd_blocked(int64_t q_rows_per_head) { return q_rows_per_head > kBwdBlockAbove; }
@@ -397,7 +400,8 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.nqblk = 1;
     p.qblk_tiles = (int32_t)nqt;
     if (bwd_blocked(Lq)) {
-        const int64_t rows_per_chunk = std::max<int64_t>(bq, kBwdBlockRows / (int64_t)lay.qmaps.size());
+        const int64_t rows_per_chunk =
+            std::max<int64_t>(bq, kBwdBlockRows / (int64_t)lay.qmaps.size());
         p.qblk_tiles = (int32_t)std::max<int64_t>(1, rows_per_chunk / bq);
         p.nqblk = (int32_t)((nqt + p.qblk_tiles - 1) / p.qblk_tiles);
     }

@@ -423,6 +423,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
         const int T = unit_steps(p, un);
         const bool kvalid = r < un.nvalid;
         const int32_t pk = kvalid ? map_pos(p.kmap[un.chunk], un.row0 + r) : 0;
+        int32_t dlo, dhi;
+        doc_range(p.docs, p.ndocs, pk, dlo, dhi);
         if (T > 0) {
             for (int g = 0; g < p.G; ++g) {
                 for (int s = 0; s < p.nq; ++s) {
@@ -430,8 +432,6 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                     if (qr.i0 >= qr.i1)
                         continue;
                     // query rows [qv, qe) of chunk qr.p see this key row
-                    int32_t dlo, dhi;
-                    doc_range(p.docs, p.ndocs, pk, dlo, dhi);
                     const int32_t qv =
                         !kvalid ? 0x7fffffff
                                 : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);

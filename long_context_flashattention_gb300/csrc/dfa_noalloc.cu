@@ -41,8 +41,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
 }  // namespace
 
 extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void* q,
@@ -52,17 +50,14 @@ extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void
 {
     if (!desc)
         return dfa::set_error(DFA_ERR_INVALID_ARG, "desc is NULL");
-    // scratch this problem needs: status word + fp32 dQ accumulator + the
-    // 32-byte -LSE/scale and -D records of every query row
-    const size_t rows = (size_t)(desc->B > 0 ? desc->B : 0) * (size_t)(desc->Hq > 0 ? desc->Hq : 0) *
-                        (size_t)(desc->N > 0 ? desc->N : 0);
-    const size_t need = kStatusBytes + align256(rows * (size_t)(desc->d > 0 ? desc->d : 0) * 4) +
-                        2 * align256(rows * 32);
+    // scratch this problem needs: the workspace of dfa_attn_bwd (status word,
+    // fp32 dQ accumulator, per-row records, and with query blocking fp32 dK
+    // and dV); an invalid descriptor is left to dfa_attn_bwd to report
+    const size_t need = dfa_workspace_size(desc, DFA_OP_BWD);
     if (need > kNoAllocScratchBytes)
         return dfa::set_error(DFA_ERR_WORKSPACE,
-                              "dfa_attn_bwd_noalloc: this problem needs %zu bytes of scratch "
-                              "(256 + B*Hq*N*(4d + 64), rounded), above the fixed %zu",
-                              need, kNoAllocScratchBytes);
+                              "dfa_attn_bwd_noalloc: this problem needs %zu bytes of scratch, "
+                              "above the fixed %zu", need, kNoAllocScratchBytes);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: no usable current device");

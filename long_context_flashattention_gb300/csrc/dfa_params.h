@@ -46,14 +46,21 @@ DFA_HD int32_t map_pos(const DevMap& m, int32_t r)
     return b + (x / m.blk) * m.blk_stride + (x % m.blk);
 }
 
+// Rows of one segment whose position is <= x.  32-bit arithmetic (positions
+// lie in [0, 2^31), base >= 0 for a non-empty segment) and no division for a
+// run of consecutive positions: the kernels evaluate this at every chunk of
+// every work unit, on the path between tensor-core steps.
 DFA_HD int32_t seg_count_le(int32_t base, int32_t len, int32_t blk, int32_t stride, int32_t x)
 {
     if (len <= 0 || x < base)
         return 0;
-    int32_t dlt = x - base;
-    int64_t runs = dlt / stride, off = dlt % stride;
-    int64_t c = runs * blk + (off + 1 < blk ? off + 1 : blk);
-    return (int32_t)(c < len ? c : len);
+    const int32_t dlt = x - base;
+    if (blk == stride)
+        return dlt < len ? dlt + 1 : len;
+    const int32_t runs = dlt / stride;
+    const int32_t off = dlt - runs * stride;
+    const int32_t c = runs * blk + (off < blk ? off + 1 : blk);
+    return c < len ? c : len;
 }
 
 // Number of rows of the chunk whose position is <= x.  Because positions

@@ -38,6 +38,12 @@ def test_workspace_sizes():
     need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32 + 2 * 32 * 131072 * 128 * 4
     assert dfa.workspace_size(d, dfa.OP_BWD) == need
     assert dfa.workspace_size(d, dfa.OP_CHUNK_BWD) == 256 + 2 * 32 * 131072 * 32
+    # blocking counts query rows per head, whatever the group size
+    g = dfa.make_desc(1, 16, 2, 16384, 64)
+    assert dfa.workspace_size(g, dfa.OP_BWD) == 256 + 16 * 16384 * 64 * 4 + 2 * 16 * 16384 * 32
+    g = dfa.make_desc(1, 2, 1, 65600, 64)
+    assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 2 * 65600 * 64 * 4 + 2 * 2 * 65600 * 32
+                                                 + 2 * 65600 * 64 * 4)
     bad = dfa.make_desc(1, 32, 32, 1000, 128, P=3)
     assert dfa.workspace_size(bad, dfa.OP_FWD) == 0
 

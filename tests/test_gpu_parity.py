@@ -449,6 +449,33 @@ def test_query_blocked_backward_ragged(orc):
     assert float((gk.double().sum(dim=2).abs() / gk.double().abs().sum(dim=2)).max()) <= G_TOL
 
 
+def test_query_blocked_backward_gqa_striped(orc):
+    """Query blocking with grouped-query heads (G = 2) on a striped partition:
+    N = 66048 > 65536 rows per head gives blocks of 32768 / 4 = 8192 rows per
+    chunk (P = 4); the key rows checked straddle position 65536, so their
+    dK/dV sum over two blocks and both query heads of the group."""
+    B, Hq, Hkv, N, d, P, kind = 1, 2, 1, 66048, 64, 4, "striped"
+    q, k, v, do = make_qkvdo(B, Hq, Hkv, N, d, seed=95)
+    perm = [dfa.permute(t.cuda(), P, kind) for t in (q, k, v, do)]
+    desc = dfa.desc_for(perm[0], perm[1], P=P, partition=kind)
+    assert dfa.workspace_size(desc, dfa.OP_BWD) > 256 + B * Hq * N * (4 * d + 64) + 255
+    o, lse = dfa.attn_fwd(*perm[:3], P=P, partition=kind)
+    g = dfa.attn_bwd(*perm[:3], o, perm[3], lse, P=P, partition=kind)
+    gq, gk, gv = (dfa.permute(t, P, kind, inverse=True) for t in g)
+    torch.cuda.synchronize()
+    krows = np.arange(65536 - 96, 65536 + 96)
+    dkr, dvr = orc.attn_bwd_kv_rows(q, k, v, do, 0, 0, krows)
+    kidx = torch.from_numpy(krows).cuda()
+    check_grad(gk[0, 0][kidx], dkr, "dK rows across blocks")
+    check_grad(gv[0, 0][kidx], dvr, "dV rows across blocks")
+    rows = np.array([0, 32767, 32768, 65535, 65536, N - 1, N + 65536] +
+                    list(np.random.default_rng(96).integers(0, Hq * N, 25)))
+    dqr, _, _ = orc.attn_bwd_q_rows(q, k, v, do, rows)
+    check_grad(gq.reshape(-1, d)[torch.from_numpy(rows).cuda()], dqr, "dQ rows")
+    sum_do = do.cuda().double().sum(dim=(1, 2))
+    assert float((gv.double().sum(dim=(1, 2)) - sum_do).norm() / sum_do.norm()) <= G_TOL
+
+
 def test_large_llama7b_32k_balanced(orc):
     _run_large(orc, "llama7b_32k", "balanced")
 
