@@ -200,3 +200,16 @@ def test_step_host_validation(L):
     fp32 = dfa.make_desc(1, 4, 2, 256, 64, o_fp32=True)
     assert L.dfa_attn_step_host(ctypes.byref(fp32), *args, 0, p, 1 << 40, None, None,
                                 None) == 2
+
+
+def test_step_host_binding_rejects_device_or_wrong_dtype():
+    """The host-buffer step takes contiguous bf16 host tensors; anything else is
+    refused before any device work."""
+    import torch
+    q = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dfa.attn_step_host(q.float(), q, q, q)
+    with pytest.raises(ValueError):
+        dfa.attn_step_host(q.transpose(2, 3), q, q, q)
+    with pytest.raises(dfa.DfaError):
+        dfa.step_host_workspace(dfa.make_desc(1, 2, 2, 64, 64), kv_heads_per_group=3)
