@@ -20,7 +20,8 @@
 //   warp 14     issues S^T = K Q^T - LSE/scale and dP^T = V dO^T - D of each
 //               step into a double-buffered TMEM pair, up to two steps ahead,
 //               so that they overlap the softmax warps' work on the previous
-//               step.  The row constants enter as one more K = 16 slice of
+//               step; S^T and dP^T signal completion separately, so the
+//               softmax warps start on P^T while dP^T is still computed.  The row constants enter as one more K = 16 slice of
 //               each product: a ones tile against per-row records holding the
 //               constant split into three bf16 values (hi + mid + lo, exact
 //               to fp32 precision), so the softmax warps read no per-row data.
@@ -83,13 +84,14 @@ struct Cfg {
     static constexpr int kQA0 = kOnes + 128 * 32;
     static constexpr int kDA0 = kQA0 + kQStages * kAugTile;
     static constexpr int kBar = kDA0 + kQStages * kAugTile;
-    // SFULL: S^T, dP^T of a step computed; PREADY: its P^T written to TMEM;
+    // SFULL: S^T of a step computed; DPFULL: its dP^T computed; PREADY: its
+    // P^T written to TMEM;
     // DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its dQ^T computed,
     // hence also its dV and dK (issued before it by the same thread), which
     // frees its P^T / dS^T; DQEMPTY: dQ^T read out of TMEM.
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
                          SFULL = QEMPTY + kQStages,  // two of each from here
-        PREADY = SFULL + 2, DSREADY = PREADY + 2, DQFULL = DSREADY + 2, DQEMPTY = DQFULL + 2,
+        DPFULL = SFULL + 2, PREADY = DPFULL + 2, DSREADY = PREADY + 2, DQFULL = DSREADY + 2, DQEMPTY = DQFULL + 2,
                          DKVFULL = DQEMPTY + 2, NBAR = DKVFULL + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t cDK = 0, cDV = D;
@@ -186,7 +188,8 @@ struct Shared {
 };
 
 // ---------------------------------------------------------------------------
-// producer (warp 9, all lanes: lane 0 issues TMA, all lanes stage LSE / D)
+// producer (warp 13; lane 0 issues every TMA load: K, V per unit, Q, dO and
+// the -LSE/scale and -D records per step)
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, const WaitCtx& w,
@@ -270,7 +273,7 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (warp 12, lane 0)
+// MMA issuers (lane 0 of warps 14 and 12)
 // ---------------------------------------------------------------------------
 // Two threads issue the MMAs, so that one thread's barrier waits (each of
 // which would otherwise leave the tensor core idle: it queues only one or
@@ -327,6 +330,7 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
             // S^T - LSE/scale: one more K = 16 slice, ones against the records
             mma_ss(tmem + C::cS(b), dOnes, sdesc_add(dQA, (m % C::kQStages) * C::kAugTile), idSt,
                    1u);
+            tc_commit(&bar[C::SFULL + b]);
             if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + b], ((m - 2) >> 1) & 1, w, 65))
                 return;
             tc_fence_after();
@@ -338,7 +342,7 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
             // dP^T - D, likewise
             mma_ss(tmem + C::cDP(b), dOnes, sdesc_add(dDA, (m % C::kQStages) * C::kAugTile), idSt,
                    1u);
-            tc_commit(&bar[C::SFULL + b]);
+            tc_commit(&bar[C::DPFULL + b]);
         }
     }
 }
@@ -401,6 +405,31 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
     }
 }
 
+// P^T for 32 query columns of one key row from its shifted scores, two
+// columns at a time (f32x2): the tensor core already subtracted LSE/scale, so
+// P = exp2((S - LSE/scale) scale log2 e).  With kMask, columns outside
+// [lo, hi) (counted from the thread's first column) are not visible to this
+// key row and get P = 0; a key row past the tile end is never visible.
+// sr receives P in fp32, pp the bf16 pairs for the tensor core.
+template <bool kMask>
+__device__ __forceinline__ void p_from_s(uint32_t* sr, uint32_t* pp, uint64_t c2x2, int lo, int hi)
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        float a0, a1;
+        f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), c2x2),
+                 a0, a1);
+        float p0 = ex2(a0), p1 = ex2(a1);
+        if (kMask) {
+            p0 = (2 * j >= lo && 2 * j < hi) ? p0 : 0.f;
+            p1 = (2 * j + 1 >= lo && 2 * j + 1 < hi) ? p1 : 0.f;
+        }
+        sr[2 * j] = __float_as_uint(p0);
+        sr[2 * j + 1] = __float_as_uint(p1);
+        pp[j] = pack_bf16x2(p0, p1);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // P^T / dS^T warpgroups (warps 0-7), one thread per key row, warpgroup h on
 // query columns [32 h, 32 h + 32) of each step; dK (h = 0) / dV (h = 1)
@@ -437,53 +466,39 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                 : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);
                     const int32_t qe = map_count_le(p.qmap[qr.p], dhi - 1);
                     for (int i = qr.i0; i < qr.i1; ++i, ++n) {
-                        const int st = n % C::kQStages;
                         const int b = n & 1;
-                        if (!mbar_wait(&bar[C::QFULL + st], (n / C::kQStages) & 1, w, 70))
-                            return;
                         if (!mbar_wait(&bar[C::SFULL + b], (n >> 1) & 1, w, 71))
                             return;
                         tc_fence_after();
                         uint32_t sr[32], dr[32];
                         tmem_ld32(tl + C::cS(b) + 32 * h, sr);
-                        tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
                         const bool full = (i >= qr.if0 && i < qr.if1) &&
                                           un.nvalid == kKvRows;
                         const int qbase = i * BQ + 32 * h;
                         tmem_ld_wait();
                         tmem_reg_fence32(sr);
-                        tmem_reg_fence32(dr);
                         // phase 1: P^T, stored and signalled first so that dV can
-                        // start while dS^T is formed
+                        // start while dS^T is formed.  Tiles that see every key
+                        // row take a path without any mask arithmetic.
                         uint32_t pp[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            // two query columns 2j, 2j+1 at a time (f32x2): the
-                            // tensor core already subtracted LSE/scale, so
-                            // P = exp2((S - LSE/scale) scale log2 e).  A row without
-                            // keys is never visible, so its P is masked.
-                            float a0, a1;
-                            f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]),
-                                                  __uint_as_float(sr[2 * j + 1])),
-                                           c2x2),
-                                     a0, a1);
-                            float p0 = ex2(a0), p1 = ex2(a1);
-                            if (!full) {
-                                const int q = qbase + 2 * j;
-                                p0 = (q >= qv && q < qe) ? p0 : 0.f;
-                                p1 = (q + 1 >= qv && q + 1 < qe) ? p1 : 0.f;
-                            }
-                            sr[2 * j] = __float_as_uint(p0);
-                            sr[2 * j + 1] = __float_as_uint(p1);
-                            pp[j] = pack_bf16x2(p0, p1);
-                        }
+                        if (full)
+                            p_from_s<false>(sr, pp, c2x2, 0, 32);
+                        else
+                            p_from_s<true>(sr, pp, c2x2, qv - qbase, qe - qbase);
                         // packed into the first 16 of this warpgroup's own 32 columns:
                         // the other warpgroup may still be reading its half
                         tmem_st16(tl + C::cS(b) + 32 * h, pp);
                         tmem_st_wait();
                         tc_fence_before();
                         mbar_arrive(&bar[C::PREADY + b]);
-                        // phase 2: dS^T = P^T (dP^T - D), D already subtracted
+                        // phase 2: dS^T = P^T (dP^T - D), D already subtracted;
+                        // dP^T completes after S^T
+                        if (!mbar_wait(&bar[C::DPFULL + b], (n >> 1) & 1, w, 70))
+                            return;
+                        tc_fence_after();
+                        tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
+                        tmem_ld_wait();
+                        tmem_reg_fence32(dr);
                         uint32_t dd[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -584,7 +599,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
 }
 
 // ---------------------------------------------------------------------------
-// dQ drain (warps 4-7): TMEM lane = feature column, columns = the step's rows
+// dQ drain (warps 8-11): TMEM lane = feature column, columns = the step's rows
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, const WaitCtx& w)
@@ -668,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar[C::SFULL + b], 1);
+            mbar_init(&bar[C::DPFULL + b], 1);
             mbar_init(&bar[C::PREADY + b], 256);
             mbar_init(&bar[C::DSREADY + b], 256);
             mbar_init(&bar[C::DQFULL + b], 1);
