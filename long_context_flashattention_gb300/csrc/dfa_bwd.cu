@@ -11,36 +11,44 @@
 // "Intra-Block vs. Inter-Block Masking Logic").
 //
 // GB300 mapping: one persistent CTA per SM, 512 threads = 4 warpgroups.  A
-// work unit is one 128-row key/value tile; it meets every visible 64-row query
-// tile ("step") of every query head of its group.  Key rows sit on TMEM lanes,
-// so dK and dV accumulate in TMEM for the whole unit.
-//   warp 13     producer: K, V once per unit (TMA); per step the Q and dO
-//               tiles and the rows' -LSE/scale and -D records (TMA) into a
-//               3-stage ring, all completing on one barrier per stage.
-//   warp 14     issues S^T = K Q^T - LSE/scale and dP^T = V dO^T - D of each
-//               step into a double-buffered TMEM pair, up to two steps ahead,
-//               so that they overlap the softmax warps' work on the previous
-//               step; S^T and dP^T signal completion separately, so the
-//               softmax warps start on P^T while dP^T is still computed.  The row constants enter as one more K = 16 slice of
-//               each product: a ones tile against per-row records holding the
-//               constant split into three bf16 values (hi + mid + lo, exact
-//               to fp32 precision), so the softmax warps read no per-row data.
-//   warp 12     issues dV += P^T dO and dK += dS^T Q (A operand read from
-//               TMEM), then dQ^T = K^T dS^T into the dP^T columns (their
-//               dS^T has been consumed by dK).  Two issuing threads keep the
-//               tensor core fed while either one waits on a barrier.
-//   warps 0-7   two warpgroups, one thread per key row, each on 32 of the
-//               step's 64 query columns: P^T = exp2(S^T c), dS^T = P^T dP^T
-//               (shifted products, packed f32x2 arithmetic), written as
-//               bf16 over S^T / dP^T and dS^T also into a double-buffered
-//               swizzled SMEM tile; at the end of a unit the first warpgroup
-//               stores dK (scaled), the second dV.
-//   warps 8-11  drain each step's dQ^T tile from TMEM into the fp32 dQ
-//               accumulator with coalesced atomics.
-//   warp 15    gives its registers to the other warpgroups.
-// TMEM columns: dK [0,d) dV [d,2d), then per buffer b: S^T [2d+128b, +64),
-// dP^T (later dQ^T) [2d+128b+64, +64).  d = 64 uses the same path: the K
-// tile is padded to 128 columns with zeros so that dQ^T has 128 lanes.
+// work unit is one 128-row key/value tile; it meets every visible 128-row
+// query tile ("step") of every query head of its group.  Key rows sit on TMEM
+// lanes, so dK and dV accumulate in TMEM for the whole unit.  Every product
+// of a step is an M = 128, N = 128 (or N = d) tcgen05 MMA: the K, V and K^T
+// operands are read from shared memory once per 128 query rows, and no
+// instruction asks shared memory for more bytes per cycle than it delivers.
+//   warp 13     producer: K, V once per unit (TMA); per step the Q tile with
+//               its rows' -LSE/scale records into a 2-stage ring, and the dO
+//               tile with its rows' -D records into a single stage that is
+//               refilled as soon as dP^T and dV of the step have read it.
+//   warp 14     issues S^T = K Q^T - LSE/scale (once dV of the previous step
+//               has consumed P^T, whose columns S^T overwrites) and
+//               dP^T = V dO^T - D (once the previous dQ^T has been drained
+//               from the columns dP^T overwrites).  The row constants enter
+//               as one more K = 16 slice of each product: a ones tile against
+//               per-row records holding the constant split into three bf16
+//               values (hi + mid + lo, exact to fp32 precision), so the
+//               softmax warps read no per-row data.  S^T and dP^T signal
+//               completion separately.
+//   warp 12     issues dV += P^T dO (on P^T ready), dK += dS^T Q (on dS^T
+//               ready; A operands read from TMEM), then dQ^T = K^T dS^T into
+//               the dP^T columns.  S^T of the next step is issued by warp 14
+//               as soon as dV completes, so it fills the tensor pipe while the
+//               softmax warps form dS^T.
+//   warps 0-7   two warpgroups, one thread per key row, warpgroup h on query
+//               columns [64 h, 64 h + 64) of each step, in two halves of 32:
+//               P^T = exp2(S^T c), packed (bf16) into its own columns of the
+//               S^T region and signalled; then dS^T = P^T (dP^T - D) packed
+//               into the dP^T region and stored into the swizzled SMEM tile
+//               that is the B operand of dQ^T.  At the end of a unit the
+//               first warpgroup stores dK (scaled), the second dV.
+//   warps 8-11  drain each step's dQ^T tile from TMEM (all 128 columns into
+//               registers, which frees the columns for the next dP^T) and add
+//               it into the fp32 dQ accumulator with coalesced atomics.
+//   warp 15     gives its registers to the other warpgroups.
+// TMEM columns: dK [0,d) dV [d,2d), S^T [2d, 2d+128), dP^T (later dQ^T)
+// [2d+128, 2d+256).  d = 64 uses the same path: the K tile is padded to 128
+// columns with zeros so that dQ^T has 128 lanes.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,50 +63,53 @@ namespace bwd {
 
 constexpr int kThreads = 512;
 // Launch: 512 threads x 128 registers = 65536.  Rebalanced per warpgroup:
-// 128 * (kRegsSoft * 2 + kRegsDrain + kRegsCtl) = 65536.
-constexpr int kRegsSoft = 152;
-constexpr int kRegsDrain = 88;
-constexpr int kRegsCtl = 120;
+// 128 * (kRegsSoft * 2 + kRegsDrain + kRegsCtl) = 65536.  The drain holds a
+// whole dQ^T row (128 values) in registers.
+constexpr int kRegsSoft = 128;
+constexpr int kRegsDrain = 160;
+constexpr int kRegsCtl = 96;
 static_assert(2 * kRegsSoft + kRegsDrain + kRegsCtl == 512, "register budget");
 constexpr int kWarpMma = 12, kWarpProducer = 13, kWarpMmaS = 14;
 constexpr int kKvRows = 128;
-constexpr int BQ = 64;  // query rows per step
+constexpr int BQ = 128;  // query rows per step
 
 template <int D>
 struct Cfg {
     static constexpr int kKTile = 128 * 128 * 2;  // K tile, always 128 columns (zero padded)
     static constexpr int kVTile = 128 * D * 2;
     static constexpr int kQTile = BQ * D * 2;     // Q or dO tile
-    static constexpr int kDsBytes = 128 * BQ * 2; // one dS^T tile
-    static constexpr int kQStages = 3;
+    static constexpr int kDsBytes = 128 * BQ * 2; // the dS^T tile (two 64-column blocks)
+    static constexpr int kQStages = 2;
+    // K = 16 slices that add -LSE/scale to S^T and -D to dP^T: a 128-row
+    // ones tile (the key side) and per stage one 128-row record tile (the
+    // query side), rows of 32 bytes, 32-byte swizzle
+    static constexpr int kAugTile = BQ * 32;
     static constexpr int kK = 0;
     static constexpr int kV = kK + kKTile;
     static constexpr int kQ0 = kV + kVTile;
-    static constexpr int kDO0 = kQ0 + kQStages * kQTile;
-    static constexpr int kDs0 = kDO0 + kQStages * kQTile;  // 2 buffers
-    // K = 16 slices that add -LSE/scale to S^T and -D to dP^T: a 128-row
-    // ones tile (the key side) and per stage one 64-row record tile for each
-    // (the query side), rows of 32 bytes, 32-byte swizzle
-    static constexpr int kAugTile = BQ * 32;
-    static constexpr int kOnes = kDs0 + 2 * kDsBytes;
+    static constexpr int kDO = kQ0 + kQStages * kQTile;
+    static constexpr int kDs = kDO + kQTile;
+    static constexpr int kOnes = kDs + kDsBytes;
     static constexpr int kQA0 = kOnes + 128 * 32;
-    static constexpr int kDA0 = kQA0 + kQStages * kAugTile;
-    static constexpr int kBar = kDA0 + kQStages * kAugTile;
+    static constexpr int kDA = kQA0 + kQStages * kAugTile;
+    static constexpr int kBar = kDA + kAugTile;
+    // KVFULL/KVEMPTY: the unit's K, V; QFULL/QEMPTY: a Q stage (with its
+    // -LSE/scale records); DOFULL/DOEMPTY: the dO stage (with its -D
+    // records; emptied by two arrivals: dP^T and dV have read it).
     // SFULL: S^T of a step computed; DPFULL: its dP^T computed; PREADY: its
-    // P^T written to TMEM;
-    // DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its dQ^T computed,
-    // hence also its dV and dK (issued before it by the same thread), which
-    // frees its P^T / dS^T; DQEMPTY: dQ^T read out of TMEM.
+    // P^T written to TMEM; PVDONE: its dV computed (P^T consumed, the S^T
+    // columns free); DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its
+    // dQ^T computed (hence its dK too, issued before it by the same thread);
+    // DQEMPTY: dQ^T read out of TMEM (the dP^T columns free).
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
-                         SFULL = QEMPTY + kQStages,  // two of each from here
-        DPFULL = SFULL + 2, PREADY = DPFULL + 2, DSREADY = PREADY + 2, DQFULL = DSREADY + 2, DQEMPTY = DQFULL + 2,
-                         DKVFULL = DQEMPTY + 2, NBAR = DKVFULL + 1;
+                         DOFULL = QEMPTY + kQStages, DOEMPTY = DOFULL + 1, SFULL = DOEMPTY + 1,
+                         DPFULL = SFULL + 1, PREADY = DPFULL + 1, PVDONE = PREADY + 1,
+                         DSREADY = PVDONE + 1, DQFULL = DSREADY + 1, DQEMPTY = DQFULL + 1,
+                         DKVFULL = DQEMPTY + 1, NBAR = DKVFULL + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
-    static constexpr uint32_t cDK = 0, cDV = D;
-    __host__ __device__ static constexpr uint32_t cS(int b) { return 2 * D + 128 * b; }
-    __host__ __device__ static constexpr uint32_t cDP(int b) { return 2 * D + 128 * b + 64; }
+    static constexpr uint32_t cDK = 0, cDV = D, cS = 2 * D, cDP = 2 * D + 128;
 };
-
+static_assert(Cfg<128>::kSmem <= 232448, "shared memory budget");
 // Query tiles of chunk p that the unit's key rows can see: [i0, i1); tiles in
 // [if0, if1) see every key row (no mask).  A key at position y is seen by the
 // queries at positions [causal ? y : doc_lo(y), doc_hi(y) - 1] (its document;
@@ -177,8 +188,10 @@ __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& u
 }
 
 // TMEM column of the packed bf16 P^T / dS^T for K step kk (16 query rows):
-// query columns [32 h, 32 h + 32) are packed at columns [32 h, 32 h + 16).
-__host__ __device__ constexpr uint32_t ptcol(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+// warpgroup h's query columns [64 h, 64 h + 64) are packed at columns
+// [64 h, 64 h + 32) of the region (its own columns, so that neither
+// warpgroup overwrites values the other has still to read).
+__host__ __device__ constexpr uint32_t ptcol(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 struct Shared {
     uint8_t* smem;
@@ -188,8 +201,8 @@ struct Shared {
 };
 
 // ---------------------------------------------------------------------------
-// producer (warp 13; lane 0 issues every TMA load: K, V per unit, Q, dO and
-// the -LSE/scale and -D records per step)
+// producer (warp 13; lane 0 issues every TMA load: K, V per unit; per step Q
+// with its -LSE/scale records, then dO with its -D records)
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, const WaitCtx& w,
@@ -241,31 +254,36 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
                 for (int i = qr.i0; i < qr.i1; ++i, ++qc) {
                     const int st = qc % C::kQStages;
                     const uint32_t use = qc / C::kQStages;
-                    if (lane == 0 && use > 0 &&
-                        !mbar_wait(&bar[C::QEMPTY + st], (use - 1) & 1, w, 51))
-                        *sh.abort_flag = 1u;
+                    const int qrow = qr.p * p.chunk_q + i * BQ;
+                    // rows past the chunk read as the next chunk's (or zeros past
+                    // the tensor); their P is masked
+                    if (lane == 0) {
+                        if (use > 0 && !mbar_wait(&bar[C::QEMPTY + st], (use - 1) & 1, w, 51))
+                            *sh.abort_flag = 1u;
+                        if (!*sh.abort_flag) {
+                            mbar_arrive_expect_tx(&bar[C::QFULL + st], C::kQTile + C::kAugTile);
+                            tma_load_3d(smem + C::kQA0 + st * C::kAugTile, tmal,
+                                        &bar[C::QFULL + st], 0, qrow, slice_q);
+#pragma unroll
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_3d(smem + C::kQ0 + st * C::kQTile + hb * (BQ * 128), tmq,
+                                            &bar[C::QFULL + st], hb * 64, qrow, slice_q);
+                        }
+                        if (!*sh.abort_flag && qc > 0 &&
+                            !mbar_wait(&bar[C::DOEMPTY], (qc - 1) & 1, w, 52))
+                            *sh.abort_flag = 1u;
+                        if (!*sh.abort_flag) {
+                            mbar_arrive_expect_tx(&bar[C::DOFULL], C::kQTile + C::kAugTile);
+                            tma_load_3d(smem + C::kDA, tmad, &bar[C::DOFULL], 0, qrow, slice_q);
+#pragma unroll
+                            for (int hb = 0; hb < D / 64; ++hb)
+                                tma_load_3d(smem + C::kDO + hb * (BQ * 128), tmdo, &bar[C::DOFULL],
+                                            hb * 64, qrow, slice_q);
+                        }
+                    }
                     __syncwarp();
                     if (*sh.abort_flag)
                         return;
-                    const int32_t m0 = i * BQ;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&bar[C::QFULL + st],
-                                              2 * C::kQTile + 2 * C::kAugTile);
-                        const int qrow = qr.p * p.chunk_q + m0;
-                        // the rows' -LSE/scale and -D records (rows past the
-                        // chunk read as zeros; their P is masked)
-                        tma_load_3d(smem + C::kQA0 + st * C::kAugTile, tmal, &bar[C::QFULL + st],
-                                    0, qrow, slice_q);
-                        tma_load_3d(smem + C::kDA0 + st * C::kAugTile, tmad, &bar[C::QFULL + st],
-                                    0, qrow, slice_q);
-#pragma unroll
-                        for (int hb = 0; hb < D / 64; ++hb) {
-                            tma_load_3d(smem + C::kQ0 + st * C::kQTile + hb * (BQ * 128), tmq,
-                                        &bar[C::QFULL + st], hb * 64, qrow, slice_q);
-                            tma_load_3d(smem + C::kDO0 + st * C::kQTile + hb * (BQ * 128), tmdo,
-                                        &bar[C::QFULL + st], hb * 64, qrow, slice_q);
-                        }
-                    }
                 }
             }
         }
@@ -275,21 +293,20 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 // ---------------------------------------------------------------------------
 // MMA issuers (lane 0 of warps 14 and 12)
 // ---------------------------------------------------------------------------
-// Two threads issue the MMAs, so that one thread's barrier waits (each of
-// which would otherwise leave the tensor core idle: it queues only one or
-// two instructions) are covered by the other's issues.  Every dependency
-// between them goes through a completion barrier, never through issue order.
+// Two threads issue the MMAs, so that one thread's barrier waits are covered
+// by the other's issues.  Every dependency between them goes through a
+// completion barrier, never through issue order.
 //
-// Warp 14 (issue_products), per step m, buffer b = m & 1:
-//   S^T(m) = K Q(m)^T    once Q(m) has landed and the products of step m-2
-//                        are complete (its dQ^T last), so that S^T(m) queues
-//                        behind dK / dQ^T(m-2), which lie on the critical
-//                        path, and runs while their dQ^T is drained;
-//   dP^T(m) = V dO(m)^T  once the dQ^T of step m-2 has left buffer b.
-// Warp 12 (issue_grads), per step n, buffer b = n & 1:
-//   dV += P^T(n) dO(n)   once the softmax warps have written P^T;
-//   dK += dS^T(n) Q(n)   once they have written dS^T (A operands from TMEM);
-//   dQ^T(n) = K^T dS^T(n) into the dP^T columns of b.
+// Warp 14 (issue_products), per step m:
+//   S^T(m) = K Q(m)^T - LSE/scale   once Q(m) has landed and dV(m-1) has
+//                                   consumed P^T(m-1) (same columns);
+//   dP^T(m) = V dO(m)^T - D         once dO(m) has landed and dQ^T(m-1) has
+//                                   been read out of the same columns.
+// Warp 12 (issue_grads), per step n:
+//   dV += P^T(n) dO(n)    once the softmax warps have written P^T (and dO(n)
+//                         has landed);
+//   dK += dS^T(n) Q(n)    once they have written dS^T (A operands from TMEM);
+//   dQ^T(n) = K^T dS^T(n) into the dP^T columns.
 template <int D>
 __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared& sh,
                                                const WaitCtx& w)
@@ -301,10 +318,10 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
     const uint64_t dKk = sdesc_sw128(smem_u32(sh.smem + C::kK), 16, 1024);
     const uint64_t dVk = sdesc_sw128(smem_u32(sh.smem + C::kV), 16, 1024);
     const uint64_t dQk = sdesc_sw128(smem_u32(sh.smem + C::kQ0), 16, 1024);
-    const uint64_t dDOk = sdesc_sw128(smem_u32(sh.smem + C::kDO0), 16, 1024);
+    const uint64_t dDOk = sdesc_sw128(smem_u32(sh.smem + C::kDO), 16, 1024);
     const uint64_t dOnes = sdesc_sw32(smem_u32(sh.smem + C::kOnes), 256);
     const uint64_t dQA = sdesc_sw32(smem_u32(sh.smem + C::kQA0), 256);
-    const uint64_t dDA = sdesc_sw32(smem_u32(sh.smem + C::kDA0), 256);
+    const uint64_t dDA = sdesc_sw32(smem_u32(sh.smem + C::kDA), 256);
     uint32_t uc = 0, m = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = bwd_unit(p, u);
@@ -315,34 +332,33 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
             return;
         ++uc;
         for (int it = 0; it < T; ++it, ++m) {
-            const int b = m & 1;
-            const uint32_t qst = (m % C::kQStages) * C::kQTile;
-            if (!mbar_wait(&bar[C::QFULL + m % C::kQStages], (m / C::kQStages) & 1, w, 61))
+            const uint32_t qs = m % C::kQStages;
+            if (!mbar_wait(&bar[C::QFULL + qs], (m / C::kQStages) & 1, w, 61))
                 return;
-            if (m >= 2 && !mbar_wait(&bar[C::DQFULL + b], ((m - 2) >> 1) & 1, w, 62))
+            if (m >= 1 && !mbar_wait(&bar[C::PVDONE], (m - 1) & 1, w, 62))
                 return;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(tmem + C::cS(b), sdesc_add(dKk, (kk >> 2) * 16384 + (kk & 3) * 32),
-                       sdesc_add(dQk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
-                       kk > 0);
+                mma_ss(tmem + C::cS, sdesc_add(dKk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(dQk, qs * C::kQTile + (kk >> 2) * (BQ * 128) + (kk & 3) * 32),
+                       idSt, kk > 0);
             // S^T - LSE/scale: one more K = 16 slice, ones against the records
-            mma_ss(tmem + C::cS(b), dOnes, sdesc_add(dQA, (m % C::kQStages) * C::kAugTile), idSt,
-                   1u);
-            tc_commit(&bar[C::SFULL + b]);
-            if (m >= 2 && !mbar_wait(&bar[C::DQEMPTY + b], ((m - 2) >> 1) & 1, w, 65))
+            mma_ss(tmem + C::cS, dOnes, sdesc_add(dQA, qs * C::kAugTile), idSt, 1u);
+            tc_commit(&bar[C::SFULL]);
+            if (!mbar_wait(&bar[C::DOFULL], m & 1, w, 64))
+                return;
+            if (m >= 1 && !mbar_wait(&bar[C::DQEMPTY], (m - 1) & 1, w, 65))
                 return;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(tmem + C::cDP(b), sdesc_add(dVk, (kk >> 2) * 16384 + (kk & 3) * 32),
-                       sdesc_add(dDOk, qst + (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt,
-                       kk > 0);
+                mma_ss(tmem + C::cDP, sdesc_add(dVk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(dDOk, (kk >> 2) * (BQ * 128) + (kk & 3) * 32), idSt, kk > 0);
             // dP^T - D, likewise
-            mma_ss(tmem + C::cDP(b), dOnes, sdesc_add(dDA, (m % C::kQStages) * C::kAugTile), idSt,
-                   1u);
-            tc_commit(&bar[C::DPFULL + b]);
+            mma_ss(tmem + C::cDP, dOnes, dDA, idSt, 1u);
+            tc_commit(&bar[C::DPFULL]);
+            tc_commit(&bar[C::DOEMPTY]);  // first of the two arrivals: dP^T has read dO
         }
     }
 }
@@ -356,9 +372,9 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
     constexpr uint32_t idKV = idesc_bf16_f32(128, D, false, true);
     constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, true, true);
     const uint64_t dQm = sdesc_sw128(smem_u32(sh.smem + C::kQ0), BQ * 128, 1024);
-    const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO0), BQ * 128, 1024);
+    const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO), BQ * 128, 1024);
     const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
-    const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs0), 16384, 1024);
+    const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs), 16384, 1024);
     uint32_t uc = 0, n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = bwd_unit(p, u);
@@ -369,37 +385,41 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
             return;
         ++uc;
         for (int it = 0; it < T; ++it, ++n) {
-            const int st = n % C::kQStages;
-            const int b = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            if (!mbar_wait(&bar[C::PREADY + b], ph, w, 63))
+            const int qs = n % C::kQStages;
+            const uint32_t ph = n & 1;
+            if (!mbar_wait(&bar[C::PREADY], ph, w, 63))
+                return;
+            // dO(n) may not have landed yet: its arrival is otherwise only
+            // waited for by dP^T(n), which can be issued after this
+            if (!mbar_wait(&bar[C::DOFULL], ph, w, 68))
                 return;
             tc_fence_after();
             // dV += P^T dO
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ts(tmem + C::cDV, tmem + C::cS(b) + ptcol(kk),
-                       sdesc_add(dDOm, st * C::kQTile + kk * 2048), idKV,
+                mma_ts(tmem + C::cDV, tmem + C::cS + ptcol(kk), sdesc_add(dDOm, kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&bar[C::PVDONE]);
+            tc_commit(&bar[C::DOEMPTY]);  // second arrival: dV has read dO
             // dK += dS^T Q
-            if (!mbar_wait(&bar[C::DSREADY + b], ph, w, 64))
+            if (!mbar_wait(&bar[C::DSREADY], ph, w, 67))
                 return;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ts(tmem + C::cDK, tmem + C::cDP(b) + ptcol(kk),
-                       sdesc_add(dQm, st * C::kQTile + kk * 2048), idKV,
+                mma_ts(tmem + C::cDK, tmem + C::cDP + ptcol(kk),
+                       sdesc_add(dQm, qs * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bar[C::QEMPTY + st]);
-            // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the dP^T columns of b
+            tc_commit(&bar[C::QEMPTY + qs]);
+            // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the dP^T columns
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tmem + C::cDP(b), sdesc_add(dKm, kk * 2048),
-                       sdesc_add(dDsm, b * C::kDsBytes + kk * 2048), idQ, kk > 0);
-            tc_commit(&bar[C::DQFULL + b]);
+                mma_ss(tmem + C::cDP, sdesc_add(dKm, kk * 2048), sdesc_add(dDsm, kk * 2048), idQ,
+                       kk > 0);
+            tc_commit(&bar[C::DQFULL]);
         }
         // all of the unit's MMAs are complete once these land: the S^T / dP^T
-        // of its last step completed before its softmax, hence before its dV
+        // of its last step completed before its softmax, hence before its dK
         tc_commit(&bar[C::DKVFULL]);
         tc_commit(&bar[C::KVEMPTY]);
     }
@@ -408,11 +428,12 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
 // P^T for 32 query columns of one key row from its shifted scores, two
 // columns at a time (f32x2): the tensor core already subtracted LSE/scale, so
 // P = exp2((S - LSE/scale) scale log2 e).  With kMask, columns outside
-// [lo, hi) (counted from the thread's first column) are not visible to this
-// key row and get P = 0; a key row past the tile end is never visible.
-// sr receives P in fp32, pp the bf16 pairs for the tensor core.
+// [lo, hi) (counted from the first of the 32) are not visible to this key row
+// and get P = 0; a key row past the tile end is never visible.  pp receives
+// the bf16 pairs.
 template <bool kMask>
-__device__ __forceinline__ void p_from_s(uint32_t* sr, uint32_t* pp, uint64_t c2x2, int lo, int hi)
+__device__ __forceinline__ void p_from_s(const uint32_t* sr, uint32_t* pp, uint64_t c2x2, int lo,
+                                         int hi)
 {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -424,15 +445,13 @@ __device__ __forceinline__ void p_from_s(uint32_t* sr, uint32_t* pp, uint64_t c2
             p0 = (2 * j >= lo && 2 * j < hi) ? p0 : 0.f;
             p1 = (2 * j + 1 >= lo && 2 * j + 1 < hi) ? p1 : 0.f;
         }
-        sr[2 * j] = __float_as_uint(p0);
-        sr[2 * j + 1] = __float_as_uint(p1);
         pp[j] = pack_bf16x2(p0, p1);
     }
 }
 
 // ---------------------------------------------------------------------------
 // P^T / dS^T warpgroups (warps 0-7), one thread per key row, warpgroup h on
-// query columns [32 h, 32 h + 32) of each step; dK (h = 0) / dV (h = 1)
+// query columns [64 h, 64 h + 64) of each step; dK (h = 0) / dV (h = 1)
 // epilogue at the end of a unit.
 // ---------------------------------------------------------------------------
 template <int D>
@@ -445,6 +464,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     const int h = warp >> 2;                 // column half of this warpgroup
     const int r = (warp & 3) * 32 + lane;    // key row inside the unit tile (TMEM lane)
     const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t tS = tl + C::cS + 64 * h, tDP = tl + C::cDP + 64 * h;
+    uint8_t* dsb = sh.smem + C::kDs + h * 16384;
     const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -466,64 +487,70 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                 : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);
                     const int32_t qe = map_count_le(p.qmap[qr.p], dhi - 1);
                     for (int i = qr.i0; i < qr.i1; ++i, ++n) {
-                        const int b = n & 1;
-                        if (!mbar_wait(&bar[C::SFULL + b], (n >> 1) & 1, w, 71))
-                            return;
-                        tc_fence_after();
-                        uint32_t sr[32], dr[32];
-                        tmem_ld32(tl + C::cS(b) + 32 * h, sr);
+                        const uint32_t ph = n & 1;
+                        // tiles that see every key row take a path without
+                        // any mask arithmetic
                         const bool full = (i >= qr.if0 && i < qr.if1) &&
                                           un.nvalid == kKvRows;
-                        const int qbase = i * BQ + 32 * h;
-                        tmem_ld_wait();
-                        tmem_reg_fence32(sr);
-                        // phase 1: P^T, stored and signalled first so that dV can
-                        // start while dS^T is formed.  Tiles that see every key
-                        // row take a path without any mask arithmetic.
-                        uint32_t pp[16];
-                        if (full)
-                            p_from_s<false>(sr, pp, c2x2, 0, 32);
-                        else
-                            p_from_s<true>(sr, pp, c2x2, qv - qbase, qe - qbase);
-                        // packed into the first 16 of this warpgroup's own 32 columns:
-                        // the other warpgroup may still be reading its half
-                        tmem_st16(tl + C::cS(b) + 32 * h, pp);
-                        tmem_st_wait();
-                        tc_fence_before();
-                        mbar_arrive(&bar[C::PREADY + b]);
-                        // phase 2: dS^T = P^T (dP^T - D), D already subtracted;
-                        // dP^T completes after S^T
-                        if (!mbar_wait(&bar[C::DPFULL + b], (n >> 1) & 1, w, 70))
+                        const int qbase = i * BQ + 64 * h;
+                        if (!mbar_wait(&bar[C::SFULL], ph, w, 71))
                             return;
                         tc_fence_after();
-                        tmem_ld32(tl + C::cDP(b) + 32 * h, dr);
-                        tmem_ld_wait();
-                        tmem_reg_fence32(dr);
-                        uint32_t dd[16];
+                        // phase 1: P^T of the 64 columns, in two halves of 32;
+                        // half c is packed into columns [16 c, 16 c + 16) of
+                        // this warpgroup's 64, which half c + 1 no longer reads
+                        uint32_t pp[32];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            float d0, d1;
-                            f2unpack(f2mul(f2pack(__uint_as_float(sr[2 * j]),
-                                                  __uint_as_float(sr[2 * j + 1])),
-                                           f2pack(__uint_as_float(dr[2 * j]),
-                                                  __uint_as_float(dr[2 * j + 1]))),
-                                     d0, d1);
-                            dd[j] = pack_bf16x2(d0, d1);
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t sr[32];
+                            tmem_ld32(tS + 32 * c, sr);
+                            tmem_ld_wait();
+                            tmem_reg_fence32(sr);
+                            if (full)
+                                p_from_s<false>(sr, pp + 16 * c, c2x2, 0, 32);
+                            else
+                                p_from_s<true>(sr, pp + 16 * c, c2x2, qv - qbase - 32 * c,
+                                               qe - qbase - 32 * c);
+                            tmem_st16(tS + 16 * c, pp + 16 * c);
                         }
-                        tmem_st16(tl + C::cDP(b) + 32 * h, dd);
-                        // the dQ MMA of step n - 2 has read dS^T buffer b
-                        if (n >= 2 && !mbar_wait(&bar[C::DQFULL + b], ((n >> 1) - 1) & 1, w, 72))
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&bar[C::PREADY]);
+                        // phase 2: dS^T = P^T (dP^T - D), D already subtracted by
+                        // the tensor core; P^T in bf16, as the dV product uses it
+                        if (!mbar_wait(&bar[C::DPFULL], ph, w, 70))
                             return;
-                        uint8_t* dsb = sh.smem + C::kDs0 + b * C::kDsBytes;
+                        tc_fence_after();
+                        // the dQ^T of step n - 1 has read the dS^T tile
+                        if (n >= 1 && !mbar_wait(&bar[C::DQFULL], (n - 1) & 1, w, 72))
+                            return;
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch)
-                            *(uint4*)(dsb + sw128_offset(r, 4 * h + ch)) =
-                                make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
-                                           dd[4 * ch + 3]);
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t dr[32], dd[16];
+                            tmem_ld32(tDP + 32 * c, dr);
+                            tmem_ld_wait();
+                            tmem_reg_fence32(dr);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const uint32_t pj = pp[16 * c + j];
+                                float d0, d1;
+                                f2unpack(f2mul(f2pack(bf16lo(pj), bf16hi(pj)),
+                                               f2pack(__uint_as_float(dr[2 * j]),
+                                                      __uint_as_float(dr[2 * j + 1]))),
+                                         d0, d1);
+                                dd[j] = pack_bf16x2(d0, d1);
+                            }
+                            tmem_st16(tDP + 16 * c, dd);
+#pragma unroll
+                            for (int ch = 0; ch < 4; ++ch)
+                                *(uint4*)(dsb + sw128_offset(r, 4 * c + ch)) =
+                                    make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
+                                               dd[4 * ch + 3]);
+                        }
                         tmem_st_wait();
                         fence_proxy_async_smem();
                         tc_fence_before();
-                        mbar_arrive(&bar[C::DSREADY + b]);
+                        mbar_arrive(&bar[C::DSREADY]);
                     }
                 }
             }
@@ -549,7 +576,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                 for (int e = 0; e < 32; ++e)
                     o[e] = 0u;
             }
-            if (kvalid && p.dkv_mode == 0) {
+            if (kvalid && p.dkv_mode == 0 &&
+                in_bounds(p.status, orow < (size_t)p.BHkv * p.Lk, 3, (long long)orow)) {
                 uint4* dst =
                     reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(outp) + orow * D + c0);
 #pragma unroll
@@ -566,11 +594,12 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
             if (p.dkv_mode != 0 && T > 0) {
                 // fp32 accumulators shared with other units of this key tile
                 // (other query blocks, other chunk-pair calls): atomic adds,
-                // made row-contiguous through one dS^T tile per warpgroup (free
-                // once the unit's products are complete): each thread stores
-                // its row's 32 values (16-byte pieces XOR-swizzled by row),
-                // then each warp adds whole rows, 128 bytes per instruction
-                float* stage = reinterpret_cast<float*>(sh.smem + C::kDs0 + h * C::kDsBytes);
+                // made row-contiguous through this warpgroup's half of the
+                // dS^T tile (free once the unit's products are complete):
+                // each thread stores its row's 32 values (16-byte pieces
+                // XOR-swizzled by row), then each warp adds whole rows, 128
+                // bytes per instruction
+                float* stage = reinterpret_cast<float*>(dsb);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     *reinterpret_cast<float4*>(stage + r * 32 + ((e ^ (r & 7)) * 4)) =
@@ -582,7 +611,9 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                 const int wq = warp & 3;
                 const size_t rbase = (size_t)un.slice * p.Lk + (size_t)un.chunk * p.chunk_k + un.row0;
                 for (int rr = wq * 32; rr < wq * 32 + 32; ++rr) {
-                    if (rr >= un.nvalid)
+                    if (rr >= un.nvalid ||
+                        !in_bounds(p.status, rbase + rr < (size_t)p.BHkv * p.Lk, 4,
+                                   (long long)(rbase + rr)))
                         break;
                     const float val = stage[rr * 32 + (((lane >> 2) ^ (rr & 7)) * 4) + (lane & 3)];
                     atomicAdd(reinterpret_cast<float*>(outp) + (rbase + rr) * D + c0 + lane, val);
@@ -590,7 +621,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                 asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
             }
         }
-        // both warpgroups staged through the shared dS^T tiles: neither may
+        // both warpgroups staged through the shared dS^T tile: neither may
         // write the next unit's dS^T before the other has finished
         if (p.dkv_mode != 0 && T > 0)
             asm volatile("bar.sync 3, 256;" ::: "memory");
@@ -608,7 +639,7 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
     uint64_t* bar = sh.bar;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = (warp & 3) * 32 + lane;
-    const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::cDP;
     const float sc = p.scale;
     uint32_t n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -623,21 +654,30 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
                 float* base =
                     p.dq_acc + ((size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q) * D + L;
                 for (int i = qr.i0; i < qr.i1; ++i, ++n) {
-                    const int b = n & 1;
-                    if (!mbar_wait(&bar[C::DQFULL + b], (n >> 1) & 1, w, 80))
+                    if (!mbar_wait(&bar[C::DQFULL], n & 1, w, 80))
                         return;
                     tc_fence_after();
-                    uint32_t v[64];
-                    tmem_ld32(tl + C::cDP(b), v);
-                    tmem_ld32(tl + C::cDP(b) + 32, v + 32);
+                    uint32_t v[128];
+                    tmem_ld32(tl, v);
+                    tmem_ld32(tl + 32, v + 32);
+                    tmem_ld32(tl + 64, v + 64);
+                    tmem_ld32(tl + 96, v + 96);
                     tmem_ld_wait();
                     tmem_reg_fence32(v);
                     tmem_reg_fence32(v + 32);
+                    tmem_reg_fence32(v + 64);
+                    tmem_reg_fence32(v + 96);
                     tc_fence_before();
-                    mbar_arrive(&bar[C::DQEMPTY + b]);
-                    if (L < D) {
-                        const int m0 = i * BQ;
-                        const int nrow = min(BQ, p.chunk_q - m0);
+                    mbar_arrive(&bar[C::DQEMPTY]);
+                    const int m0 = i * BQ;
+                    const int nrow = min(BQ, p.chunk_q - m0);
+                    // rows [m0, m0 + nrow) of chunk qr.p of query head slice_q
+                    if (L < D &&
+                        in_bounds(p.status,
+                                  m0 >= 0 && nrow > 0 && qr.p < p.nq &&
+                                      (size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q + m0 +
+                                              nrow <= (size_t)p.BHkv * p.G * p.Lq,
+                                  5, (long long)slice_q * p.Lq + qr.p * p.chunk_q + m0)) {
                         if (nrow == BQ) {
 #pragma unroll
                             for (int c = 0; c < BQ; ++c)
@@ -681,14 +721,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[C::QFULL + s], 1);
             mbar_init(&bar[C::QEMPTY + s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bar[C::SFULL + b], 1);
-            mbar_init(&bar[C::DPFULL + b], 1);
-            mbar_init(&bar[C::PREADY + b], 256);
-            mbar_init(&bar[C::DSREADY + b], 256);
-            mbar_init(&bar[C::DQFULL + b], 1);
-            mbar_init(&bar[C::DQEMPTY + b], 128);
-        }
+        mbar_init(&bar[C::DOFULL], 1);
+        mbar_init(&bar[C::DOEMPTY], 2);
+        mbar_init(&bar[C::SFULL], 1);
+        mbar_init(&bar[C::DPFULL], 1);
+        mbar_init(&bar[C::PREADY], 256);
+        mbar_init(&bar[C::PVDONE], 1);
+        mbar_init(&bar[C::DSREADY], 256);
+        mbar_init(&bar[C::DQFULL], 1);
+        mbar_init(&bar[C::DQEMPTY], 128);
         mbar_init(&bar[C::DKVFULL], 1);
         fence_barrier_init();
     }
@@ -733,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_products<D>(p, sh, wctx);
         }
     } else if (warp >= 8) {
-        reg_dealloc<kRegsDrain>();
+        reg_alloc<kRegsDrain>();
         dq_drain<D>(p, sh, wctx);
     } else {
         reg_alloc<kRegsSoft>();

@@ -439,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i)
                             o[i] = 0u;
                     }
-                    if (valid) {
+                    if (valid && in_bounds(p.status, orow < (size_t)p.BH * p.Lq, 1,
+                                           (long long)orow)) {
                         if (p.o_fp32) {
                             float4* dst = reinterpret_cast<float4*>(
                                 reinterpret_cast<float*>(p.o) + orow * D + c0);
@@ -466,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (valid)
+                if (valid && in_bounds(p.status, orow < (size_t)p.BH * p.Lq, 2, (long long)orow))
                     p.lse[orow] = (l > 0.f) ? (m_ref * p.scale + lg2(l) * 0.69314718055994531f)
                                             : -INFINITY;
                 tc_fence_before();

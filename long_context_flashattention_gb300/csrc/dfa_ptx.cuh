@@ -29,6 +29,31 @@ struct DevStatus {
 };
 
 constexpr int kStatusTimeout = 5;  // == DFA_ERR_TIMEOUT
+constexpr int kStatusBounds = 6;   // == DFA_ERR_BOUNDS
+
+// Index checks of the bounds-checking build (compiled with DFA_DEBUG_BOUNDS):
+// in_bounds(st, ok, site, idx) returns ok; when it is false the first
+// violation's site and index are recorded in the status word and the caller
+// skips the access.  In the normal build it is the constant true.
+#ifdef DFA_DEBUG_BOUNDS
+__device__ __noinline__ static bool bounds_fail(DevStatus* st, int site, long long idx)
+{
+    if (st && atomicCAS(&st->code, 0, kStatusBounds) == 0) {
+        st->where = site;
+        st->detail = (int)(idx > 0x7fffffffll ? 0x7fffffffll : idx);
+    }
+    return false;
+}
+__device__ __forceinline__ bool in_bounds(DevStatus* st, bool ok, int site, long long idx)
+{
+    return ok ? true : bounds_fail(st, site, idx);
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(DevStatus*, bool, int, long long)
+{
+    return true;
+}
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {

@@ -15,13 +15,15 @@ import re
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdfa.so")
+# DFA_DEBUG_BOUNDS=1 loads the bounds-checking build of the library instead
+DEBUG_BOUNDS = os.environ.get("DFA_DEBUG_BOUNDS") == "1"
+LIB_PATH = os.path.join(_PKG, "libdfa_bounds.so" if DEBUG_BOUNDS else "libdfa.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "dfa.h")
 
 PARTITIONS = {"contiguous": 0, "balanced": 1, "striped": 2}
 OP_FWD, OP_BWD, OP_CHUNK_FWD, OP_CHUNK_BWD, OP_RING_FWD = 0, 1, 2, 3, 4
 STATUS = {0: "DFA_OK", 1: "DFA_ERR_INVALID_ARG", 2: "DFA_ERR_UNSUPPORTED",
-          3: "DFA_ERR_WORKSPACE", 4: "DFA_ERR_CUDA", 5: "DFA_ERR_TIMEOUT"}
+          3: "DFA_ERR_WORKSPACE", 4: "DFA_ERR_CUDA", 5: "DFA_ERR_TIMEOUT", 6: "DFA_ERR_BOUNDS"}
 
 
 class DfaError(RuntimeError):
@@ -53,11 +55,35 @@ class RingWorker(ctypes.Structure):
                 ("kv_slots", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
 
 
+class HostStep(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("dout", ctypes.c_void_p), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p)]
+
+
+class SchedPair(ctypes.Structure):
+    _fields_ = [("worker", ctypes.c_int32), ("step", ctypes.c_int32),
+                ("kv_worker", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("tokens", ctypes.c_int64), ("first_item", ctypes.c_int64),
+                ("n_items", ctypes.c_int64)]
+
+
+class SchedItem(ctypes.Structure):
+    _fields_ = [("worker", ctypes.c_int32), ("step", ctypes.c_int32), ("q_tile", ctypes.c_int32),
+                ("kv_begin", ctypes.c_int32), ("kv_end", ctypes.c_int32),
+                ("mask_class", ctypes.c_int32)]
+
+
 class Schedule(ctypes.Structure):
     _fields_ = [("pair_tokens", ctypes.POINTER(ctypes.c_int64)),
                 ("tile_counts", ctypes.POINTER(ctypes.c_int64)),
                 ("total_pairs", ctypes.c_int64), ("eta_slots", ctypes.c_double),
-                ("eta_flops", ctypes.c_double)]
+                ("eta_flops", ctypes.c_double), ("pairs", ctypes.POINTER(SchedPair)),
+                ("items", ctypes.POINTER(SchedItem)), ("capacity", ctypes.c_int64),
+                ("n_items", ctypes.c_int64)]
+
+
+TILE_SKIP, TILE_FULL, TILE_PARTIAL = 0, 1, 2
 
 
 _lib = None
@@ -68,8 +94,8 @@ def lib():
     global _lib
     if _lib is None:
         from . import build as _build
-        if not _build.up_to_date():
-            _build.build()
+        if not _build.up_to_date(debug_bounds=DEBUG_BOUNDS):
+            _build.build(debug_bounds=DEBUG_BOUNDS)
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libdfa.so not found at {LIB_PATH}; run build()")
         L = ctypes.CDLL(LIB_PATH)
@@ -90,6 +116,8 @@ def lib():
             "dfa_attn_step_host_workspace_size": (sz, [D, i32]),
             "dfa_attn_step_host": (i32, [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp,
                                          vp, vp]),
+            "dfa_attn_steps_host": (i32, [D, i32, ctypes.POINTER(HostStep), i32, vp, sz, vp, vp,
+                                          vp]),
             "dfa_decode_workspace_size": (sz, [D, i32, i64, i32]),
             "dfa_decode": (i32, [D, i32, i64, i64, vp, vp, vp, vp, vp, i32, vp, sz, vp]),
             "dfa_make_schedule": (i32, [D, i32, i32, ctypes.POINTER(Schedule)]),
@@ -445,23 +473,87 @@ def attn_step_host(q, k, v, dout, causal=True, scale=None, P=1, partition="conti
     return outs
 
 
+def attn_steps_host(steps, causal=True, scale=None, P=1, partition="contiguous", stripe=1,
+                    docs=None, kv_heads_per_group=0, outs=None, ws=None, overlap=True,
+                    stream=None, h2d_stream=None, d2h_stream=None):
+    """Several steps from host memory in one call (dfa_attn_steps_host): steps
+    is a list of (q, k, v, dout) bf16 host tensors of one shape; outs a list of
+    (o, lse, dq, dk, dv) host tensors per step (allocated pinned when None).
+    Returns outs."""
+    if not steps:
+        raise ValueError("need at least one step")
+    q0, k0 = steps[0][0], steps[0][1]
+    for st in steps:
+        for t, ref in zip(st, steps[0]):
+            if (t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or
+                    t.shape != ref.shape):
+                raise ValueError("steps must be contiguous bf16 host tensors of one shape")
+    desc = desc_for(q0, k0, causal=causal, scale=scale, P=P, partition=partition, stripe=stripe,
+                    docs=docs)
+    B, Hq, N, d = q0.shape
+    Hkv = k0.shape[1]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if outs is None:
+        def pinned(*shape, dtype=torch.bfloat16):
+            return torch.empty(*shape, dtype=dtype, pin_memory=True)
+        outs = [(pinned(B, Hq, N, d), pinned(B, Hq, N, dtype=torch.float32), pinned(B, Hq, N, d),
+                 pinned(B, Hkv, N, d), pinned(B, Hkv, N, d)) for _ in steps]
+    if len(outs) != len(steps):
+        raise ValueError("one output set per step")
+    for o in outs:
+        for t in o:
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("outputs must be contiguous host tensors")
+    if ws is None:
+        ws = step_host_workspace(desc, kv_heads_per_group, dev)
+    if overlap:
+        h2d_stream = h2d_stream or _up_streams.setdefault(dev, torch.cuda.Stream(dev))
+        d2h_stream = d2h_stream or _down_streams.setdefault(dev, torch.cuda.Stream(dev))
+    arr = (HostStep * len(steps))(*[
+        HostStep(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), o.data_ptr(),
+                 l.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+        for (q, k, v, do), (o, l, dq, dk, dv) in zip(steps, outs)])
+    _check(lib().dfa_attn_steps_host(ctypes.byref(desc), len(steps), arr, kv_heads_per_group,
+                                     _ptr(ws), ws.numel(), _stream(stream),
+                                     _stream(h2d_stream) if overlap else None,
+                                     _stream(d2h_stream) if overlap else None))
+    return outs
+
+
 # ----------------------------------------------------------------------------
 # host-only helpers
 # ----------------------------------------------------------------------------
-def make_schedule(N, P, partition="contiguous", stripe=1, tile_m=128, tile_n=128, causal=True):
-    """Ring schedule loads (host only): returns dict with pair_tokens [P][P]
-    (worker, step), tile_counts [P][P][3], total_pairs, eta_slots, eta_flops."""
+def make_schedule(N, P, partition="contiguous", stripe=1, tile_m=128, tile_n=128, causal=True,
+                  items=True):
+    """Ring schedule (host only, dfa_make_schedule): returns a dict with
+    pair_tokens [P][P] (worker, step), tile_counts [P][P][3], total_pairs,
+    eta_slots, eta_flops, the pair list ``pairs`` [P*P] of (worker, step,
+    kv_worker, tokens, first_item, n_items) and, with items=True, the tile
+    work items [n_items] of (worker, step, q_tile, kv_begin, kv_end,
+    mask_class) -- sized by a first call with capacity 0."""
     import numpy as np
     desc = make_desc(1, 1, 1, N, 64, causal=causal, P=P, partition=partition, stripe=stripe)
     pt = (ctypes.c_int64 * (P * P))()
     tc = (ctypes.c_int64 * (3 * P * P))()
+    pr = (SchedPair * (P * P))()
     s = Schedule(ctypes.cast(pt, ctypes.POINTER(ctypes.c_int64)),
-                 ctypes.cast(tc, ctypes.POINTER(ctypes.c_int64)), 0, 0.0, 0.0)
+                 ctypes.cast(tc, ctypes.POINTER(ctypes.c_int64)), 0, 0.0, 0.0,
+                 ctypes.cast(pr, ctypes.POINTER(SchedPair)), None, 0, 0)
     _check(lib().dfa_make_schedule(ctypes.byref(desc), tile_m, tile_n, ctypes.byref(s)))
-    return {"pair_tokens": np.array(pt[:], dtype=np.int64).reshape(P, P),
-            "tile_counts": np.array(tc[:], dtype=np.int64).reshape(P, P, 3),
-            "total_pairs": int(s.total_pairs), "eta_slots": float(s.eta_slots),
-            "eta_flops": float(s.eta_flops)}
+    out = {"pair_tokens": np.array(pt[:], dtype=np.int64).reshape(P, P),
+           "tile_counts": np.array(tc[:], dtype=np.int64).reshape(P, P, 3),
+           "total_pairs": int(s.total_pairs), "eta_slots": float(s.eta_slots),
+           "eta_flops": float(s.eta_flops), "n_items": int(s.n_items),
+           "pairs": np.array([(x.worker, x.step, x.kv_worker, x.tokens, x.first_item, x.n_items)
+                              for x in pr], dtype=np.int64)}
+    if items:
+        it = (SchedItem * max(1, s.n_items))()
+        s.items = ctypes.cast(it, ctypes.POINTER(SchedItem))
+        s.capacity = s.n_items
+        _check(lib().dfa_make_schedule(ctypes.byref(desc), tile_m, tile_n, ctypes.byref(s)))
+        out["items"] = np.array([(x.worker, x.step, x.q_tile, x.kv_begin, x.kv_end, x.mask_class)
+                                 for x in it[:s.n_items]], dtype=np.int64).reshape(-1, 6)
+    return out
 
 
 def stream_status(ws, stream=None) -> int:
