@@ -59,7 +59,10 @@ typedef enum dfa_status {
     DFA_ERR_UNSUPPORTED = 2, /* valid but not implemented (d, alignment, map) */
     DFA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
     DFA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed             */
-    DFA_ERR_TIMEOUT = 5      /* a device-side wait gave up (async, see above) */
+    DFA_ERR_TIMEOUT = 5,     /* a device-side wait gave up (async, see above) */
+    DFA_ERR_BOUNDS = 6       /* a device-side index outside its tensor: only a
+                                library built with DFA_DEBUG_BOUNDS checks and
+                                reports this (async, like DFA_ERR_TIMEOUT)    */
 } dfa_status;
 
 /* Sequence partitions over P logical workers (chunks). */
@@ -289,6 +292,35 @@ dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* h_q, const 
                               void* h2d_stream, void* d2h_stream);
 
 /*
+ * dfa_attn_steps_host -- nsteps consecutive steps of dfa_attn_step_host in
+ * one call (at most 64): the same work and results as nsteps calls, but the
+ * (step, group) items form one stream, so the first groups of step t + 1
+ * upload while the last groups of step t compute and download.  Only the
+ * first upload and the last download of the whole call are left unhidden.
+ * steps[t] holds step t's host tensors, with the layouts and rules of
+ * dfa_attn_step_host (the same buffers may serve several steps when the
+ * caller expects them to be overwritten in step order).  Same workspace as
+ * dfa_attn_step_host.  The pages describe no counterpart: this is the
+ * host-streaming executor's loop over training steps.
+ */
+typedef struct dfa_host_step {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dout;
+    void* o;
+    float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+} dfa_host_step;
+
+dfa_status dfa_attn_steps_host(const dfa_attn_desc* desc, int32_t nsteps,
+                               const dfa_host_step* steps, int32_t kv_heads_per_group,
+                               void* ws, size_t ws_bytes, void* compute_stream,
+                               void* h2d_stream, void* d2h_stream);
+
+/*
  * dfa_decode -- split-KV decoding: T query tokens per sequence against L
  * cached keys (FlashAttention glossary entry, the Flash-Decoding variant:
  * the keys are cut into splits of split_len, each split gives a normalised
@@ -342,24 +374,74 @@ dfa_status dfa_permute_rope(const dfa_attn_desc* desc, int32_t inverse, const vo
                             void* out, int64_t heads, float theta_base, void* stream);
 
 /*
- * Ring schedule (host only, no device work).  For the P workers of desc's
- * partition: pair_tokens[p*P + s] = visible causal (query, key) token pairs of
- * worker p at ring step s, when it holds the keys of worker (p - s) mod P
- * (Striped Attention Guide, "Workload Balance Theorem"; DistFlashAttn Guide,
- * "The Causal Imbalance Crisis").  Tiles are tile_m query rows by tile_n key
- * rows inside each chunk pair; tile_counts[(p*P + s)*3 + c] counts tiles of
- * class c = 0 skipped, 1 full (no mask), 2 partial (element mask).
- * eta_slots = non-empty (p, s) slots / P^2 (the pages' eta_util);
- * eta_flops = total pairs / (P * sum_s max_p pair_tokens) (lockstep
- * utilisation).  Buffers are caller-owned host arrays of P*P and 3*P*P
- * int64.
+ * Ring schedule (host only, no device work) for the P workers of desc's
+ * partition (Striped Attention Guide, "Workload Balance Theorem": at ring
+ * step s worker p holds the keys of worker (p - s) mod P; "Intra-Block vs.
+ * Inter-Block Masking Logic": a tile pair is skipped, computed without a mask
+ * or computed with an element mask; DistFlashAttn Guide, "The Causal
+ * Imbalance Crisis" and "The Folded Chunk Assignment").  Causal masking by
+ * global position only: desc's documents are not taken into account.
+ *
+ * The query rows of a worker's chunk are cut into tiles of tile_m rows, the
+ * key rows into tiles of tile_n rows (the last tile of each may be short).
+ * Because positions increase along every chunk, the key tiles that a query
+ * tile sees form a prefix of the key chunk, and the ones it sees without a
+ * mask a shorter prefix; so the tile pairs of a query tile are at most three
+ * work items, each a range of key tiles of one class:
+ *   DFA_TILE_FULL     [0, full)      every (query, key) pair visible
+ *   DFA_TILE_PARTIAL  [full, vis)    an element mask is needed
+ *   DFA_TILE_SKIP     [vis, nkt)     no pair visible (never computed)
+ * (non-causal: one FULL item [0, nkt)).  Empty ranges give no item.
+ *
+ * Outputs (all caller-owned host memory; any array pointer may be NULL to
+ * skip that output):
+ *   pair_tokens[p*P + s]     visible (query, key) token pairs of worker p at
+ *                            step s;
+ *   tile_counts[(p*P + s)*3 + c]  tiles of class c (0 skip, 1 full,
+ *                            2 partial) of that pair;
+ *   pairs[p*P + s]           the pair list: worker, step, the key/value
+ *                            worker it holds, its tokens and the range of
+ *                            its work items in items[];
+ *   items[0 .. n_items)      the tile work items, pair by pair (p major,
+ *                            then s), query tile by query tile, in class
+ *                            order FULL, PARTIAL, SKIP;
+ *   total_pairs, eta_slots = non-empty (p, s) slots / P^2 (the pages'
+ *   eta_util), eta_flops = total pairs / (P * sum_s max_p pair_tokens)
+ *   (lockstep utilisation).
+ * Item buffer protocol: n_items is always set to the number of items the
+ * schedule has.  capacity = 0 (or items = NULL) is a size query: nothing is
+ * written to items.  0 < capacity < n_items returns DFA_ERR_INVALID_ARG.
  */
+enum { DFA_TILE_SKIP = 0, DFA_TILE_FULL = 1, DFA_TILE_PARTIAL = 2 };
+
+typedef struct dfa_sched_pair {
+    int32_t worker;     /* p: holds the query chunk of worker p            */
+    int32_t step;       /* s: ring step                                    */
+    int32_t kv_worker;  /* (p - s) mod P: whose keys/values it holds        */
+    int32_t reserved;
+    int64_t tokens;     /* visible (query, key) token pairs                */
+    int64_t first_item; /* index of the pair's first item in items[]       */
+    int64_t n_items;    /* number of items of the pair                     */
+} dfa_sched_pair;
+
+typedef struct dfa_sched_item {
+    int32_t worker, step; /* the pair                                      */
+    int32_t q_tile;       /* query tile index inside the worker's chunk    */
+    int32_t kv_begin;     /* key tile range [kv_begin, kv_end) inside the  */
+    int32_t kv_end;       /*   key/value chunk                             */
+    int32_t mask_class;   /* DFA_TILE_FULL / DFA_TILE_PARTIAL / DFA_TILE_SKIP */
+} dfa_sched_item;
+
 typedef struct dfa_schedule {
-    int64_t* pair_tokens;
-    int64_t* tile_counts;
+    int64_t* pair_tokens;   /* [P*P] or NULL                               */
+    int64_t* tile_counts;   /* [P*P*3] or NULL                             */
     int64_t total_pairs;
     double eta_slots;
     double eta_flops;
+    dfa_sched_pair* pairs;  /* [P*P] or NULL                               */
+    dfa_sched_item* items;  /* [capacity] or NULL                          */
+    int64_t capacity;       /* in: items[] capacity (0: size query)        */
+    int64_t n_items;        /* out: items of the schedule                  */
 } dfa_schedule;
 
 dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t tile_n,
@@ -400,7 +482,9 @@ size_t dfa_workspace_size(const dfa_attn_desc* desc, int32_t op);
 /*
  * Synchronise stream, then read and clear the device status word in ws.
  * Returns DFA_OK, DFA_ERR_TIMEOUT (a kernel gave up waiting; its outputs are
- * invalid) or DFA_ERR_CUDA (the stream reported an error).
+ * invalid), DFA_ERR_BOUNDS (bounds-checking build only: a kernel computed an
+ * index outside a tensor and skipped that access) or DFA_ERR_CUDA (the
+ * stream reported an error).
  */
 dfa_status dfa_stream_status(void* ws, void* stream);
 

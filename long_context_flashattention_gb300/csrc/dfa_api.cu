@@ -515,6 +515,8 @@ const char* dfa_status_string(dfa_status s)
         return "CUDA error";
     case DFA_ERR_TIMEOUT:
         return "device wait timed out";
+    case DFA_ERR_BOUNDS:
+        return "device index out of bounds (bounds-checking build)";
     }
     return "unknown status";
 }
@@ -872,16 +874,36 @@ dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t 
     dfa_status s = check_desc(desc, true);
     if (s != DFA_OK)
         return s;
-    if (!out || !out->pair_tokens || !out->tile_counts)
-        return fail(DFA_ERR_INVALID_ARG, "schedule buffers are NULL");
+    if (!out)
+        return fail(DFA_ERR_INVALID_ARG, "schedule output is NULL");
     if (tile_m < 1 || tile_n < 1)
         return fail(DFA_ERR_INVALID_ARG, "tile sizes must be positive");
+    if (out->capacity < 0)
+        return fail(DFA_ERR_INVALID_ARG, "item capacity must be >= 0");
     const int P = desc->P;
     const int32_t n = (int32_t)(desc->N / P);
+    const int32_t nqt = (n + tile_m - 1) / tile_m, nkt = (n + tile_n - 1) / tile_n;
     std::vector<DevMap> maps(P);
     for (int p = 0; p < P; ++p)
         maps[p] = to_dev(partition_map(*desc, p));
-    int64_t total = 0;
+    // Key tiles [0, vis) of the kv chunk are seen by query tile qt, tiles
+    // [0, full) by every row of it (positions increase along each chunk, so
+    // both sets are prefixes).
+    auto tile_prefixes = [&](const DevMap& qm, const DevMap& km, int32_t qt, int32_t& vis,
+                             int32_t& full) {
+        if (!desc->causal) {
+            vis = full = nkt;
+            return;
+        }
+        const int32_t q0 = qt * tile_m, q1 = std::min(n, q0 + tile_m) - 1;
+        const int32_t cmax = map_count_le(km, map_pos(qm, q1));
+        const int32_t cmin = map_count_le(km, map_pos(qm, q0));
+        vis = (cmax + tile_n - 1) / tile_n;
+        full = (cmin == n) ? nkt : cmin / tile_n;
+    };
+    // pass 1: loads, tile counts and the number of items
+    std::vector<int64_t> tokens((size_t)P * P), counts((size_t)P * P * 3), nitems((size_t)P * P);
+    int64_t total = 0, items_total = 0;
     for (int p = 0; p < P; ++p) {
         for (int st = 0; st < P; ++st) {
             const int w = ((p - st) % P + P) % P;
@@ -894,28 +916,72 @@ dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t 
             } else {
                 pairs = (int64_t)n * n;
             }
-            out->pair_tokens[p * P + st] = pairs;
+            const size_t ps = (size_t)p * P + st;
+            tokens[ps] = pairs;
             total += pairs;
-            int64_t cnt[3] = {0, 0, 0};
-            const int32_t nkt = (n + tile_n - 1) / tile_n;
-            for (int32_t q0 = 0; q0 < n; q0 += tile_m) {
-                const int32_t q1 = std::min(n, q0 + tile_m) - 1;
-                int32_t vis_tiles, full_tiles;
-                if (desc->causal) {
-                    const int32_t cmax = map_count_le(km, map_pos(qm, q1));
-                    const int32_t cmin = map_count_le(km, map_pos(qm, q0));
-                    vis_tiles = (cmax + tile_n - 1) / tile_n;
-                    full_tiles = (cmin == n) ? nkt : cmin / tile_n;
-                } else {
-                    vis_tiles = nkt;
-                    full_tiles = nkt;
-                }
-                cnt[0] += nkt - vis_tiles;
-                cnt[1] += full_tiles;
-                cnt[2] += vis_tiles - full_tiles;
+            int64_t cnt[3] = {0, 0, 0}, ni = 0;
+            for (int32_t qt = 0; qt < nqt; ++qt) {
+                int32_t vis, full;
+                tile_prefixes(qm, km, qt, vis, full);
+                cnt[DFA_TILE_SKIP] += nkt - vis;
+                cnt[DFA_TILE_FULL] += full;
+                cnt[DFA_TILE_PARTIAL] += vis - full;
+                ni += (full > 0) + (vis > full) + (nkt > vis);
             }
             for (int c = 0; c < 3; ++c)
-                out->tile_counts[(p * P + st) * 3 + c] = cnt[c];
+                counts[ps * 3 + c] = cnt[c];
+            nitems[ps] = ni;
+            items_total += ni;
+        }
+    }
+    out->n_items = items_total;
+    const bool write_items = out->items != nullptr && out->capacity > 0;
+    if (write_items && out->capacity < items_total)
+        return fail(DFA_ERR_INVALID_ARG, "item buffer too small: %lld < %lld",
+                    (long long)out->capacity, (long long)items_total);
+    // pass 2: outputs
+    int64_t first = 0;
+    for (int p = 0; p < P; ++p) {
+        for (int st = 0; st < P; ++st) {
+            const int w = ((p - st) % P + P) % P;
+            const size_t ps = (size_t)p * P + st;
+            if (out->pair_tokens)
+                out->pair_tokens[ps] = tokens[ps];
+            if (out->tile_counts)
+                for (int c = 0; c < 3; ++c)
+                    out->tile_counts[ps * 3 + c] = counts[ps * 3 + c];
+            if (out->pairs) {
+                dfa_sched_pair& pr = out->pairs[ps];
+                pr.worker = p;
+                pr.step = st;
+                pr.kv_worker = w;
+                pr.reserved = 0;
+                pr.tokens = tokens[ps];
+                pr.first_item = first;
+                pr.n_items = nitems[ps];
+            }
+            if (write_items) {
+                int64_t k = first;
+                for (int32_t qt = 0; qt < nqt; ++qt) {
+                    int32_t vis, full;
+                    tile_prefixes(maps[p], maps[w], qt, vis, full);
+                    const int32_t rb[3][3] = {{0, full, DFA_TILE_FULL},
+                                              {full, vis, DFA_TILE_PARTIAL},
+                                              {vis, nkt, DFA_TILE_SKIP}};
+                    for (const auto& r : rb) {
+                        if (r[1] <= r[0])
+                            continue;
+                        dfa_sched_item& it = out->items[k++];
+                        it.worker = p;
+                        it.step = st;
+                        it.q_tile = qt;
+                        it.kv_begin = r[0];
+                        it.kv_end = r[1];
+                        it.mask_class = r[2];
+                    }
+                }
+            }
+            first += nitems[ps];
         }
     }
     out->total_pairs = total;
@@ -923,7 +989,7 @@ dfa_status dfa_make_schedule(const dfa_attn_desc* desc, int32_t tile_m, int32_t 
     for (int st = 0; st < P; ++st) {
         int64_t mx = 0;
         for (int p = 0; p < P; ++p) {
-            const int64_t v = out->pair_tokens[p * P + st];
+            const int64_t v = tokens[(size_t)p * P + st];
             if (v > 0)
                 ++nonempty;
             mx = std::max(mx, v);

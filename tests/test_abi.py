@@ -137,6 +137,69 @@ def test_schedule_bit_exact_against_oracle(orc, kind, N, P, stripe, tiles):
     assert abs(s["eta_slots"] - nonempty / P**2) < 1e-15
 
 
+@pytest.mark.parametrize("kind,N,P,stripe", [("contiguous", 256, 4, 1), ("balanced", 256, 4, 1),
+                                             ("striped", 256, 4, 1), ("striped", 1024, 4, 64),
+                                             ("balanced", 2048, 8, 1), ("striped", 2048, 8, 1),
+                                             ("contiguous", 2048, 8, 1), ("striped", 2048, 4, 64)])
+@pytest.mark.parametrize("tiles", [(64, 64), (128, 128), (256, 128), (96, 64)])
+def test_schedule_items_bit_exact_against_oracle(orc, kind, N, P, stripe, tiles):
+    """The pair list and the tile work items of dfa_make_schedule, expanded
+    back to one class per (query tile, key tile), equal the oracle's brute-force
+    classification of every chunk pair (Striped Attention Guide, "Workload
+    Balance Theorem" and "Intra-Block vs. Inter-Block Masking Logic")."""
+    tm, tn = tiles
+    s = dfa.make_schedule(N, P, kind, stripe, tile_m=tm, tile_n=tn)
+    cnt = orc.pair_counts(kind, N, P, stripe)
+    items, pairs = s["items"], s["pairs"]
+    assert len(items) == s["n_items"] and len(pairs) == P * P
+    n = N // P
+    nqt, nkt = -(-n // tm), -(-n // tn)
+    first = 0
+    for p in range(P):
+        for st in range(P):
+            w = (p - st) % P
+            worker, step, kvw, tokens, f, k = pairs[p * P + st]
+            assert (worker, step, kvw, tokens) == (p, st, w, cnt[p, w])
+            assert f == first
+            first += k
+            cls = np.full((nqt, nkt), -1, dtype=np.int64)
+            for it in items[f:f + k]:
+                iw, ist, qt, kb, ke, c = it
+                assert (iw, ist) == (p, st) and 0 <= kb < ke <= nkt
+                assert (cls[qt, kb:ke] == -1).all()      # items do not overlap
+                cls[qt, kb:ke] = c
+            assert np.array_equal(cls, orc.tile_classes(kind, N, P, p, w, tm, tn, stripe))
+    assert first == s["n_items"]
+
+
+def test_schedule_item_capacity_protocol():
+    L = dfa.lib()
+    desc = dfa.make_desc(1, 1, 1, 1024, 64, P=4, partition="striped")
+    q = dfa.Schedule()
+    assert L.dfa_make_schedule(ctypes.byref(desc), 128, 128, ctypes.byref(q)) == 0
+    need = q.n_items
+    assert need > 0
+    small = (dfa.SchedItem * (need - 1))()
+    q.items = ctypes.cast(small, ctypes.POINTER(dfa.SchedItem))
+    q.capacity = need - 1
+    assert L.dfa_make_schedule(ctypes.byref(desc), 128, 128, ctypes.byref(q)) == 1
+    assert q.n_items == need
+    q.capacity = -1
+    assert L.dfa_make_schedule(ctypes.byref(desc), 128, 128, ctypes.byref(q)) == 1
+    non_causal = dfa.make_schedule(1024, 4, "striped", causal=False)
+    assert (non_causal["items"][:, 5] == dfa.TILE_FULL).all()
+    assert len(non_causal["items"]) == 16 * (1024 // 4 // 128)
+
+
+def test_sample_key_rows_covers_the_fixed_rows():
+    from long_context_flashattention_gb300.inputs import sample_key_rows
+    r = sample_key_rows(131072, 8, 4096, seed=5)
+    assert len(r) == 4096 and r == sorted(set(r)) and r == sample_key_rows(131072, 8, 4096, 5)
+    for x in (0, 1, 127, 128, 16383, 16384, 8191, 8192, 32767, 32768, 131071):
+        assert x in r
+    assert len(sample_key_rows(256, 4, 4096, seed=5)) == 256
+
+
 def test_schedule_eta_closed_forms():
     # contiguous: (P+1)/(2P) non-empty slots; folded and striped keep every slot busy
     for P in (2, 4, 8):
