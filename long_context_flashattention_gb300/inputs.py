@@ -94,6 +94,24 @@ def sample_rows(B: int, H: int, N: int, count: int, seed: int, chunk: int | None
     return sorted(set(fixed + rnd))[:max(count, len(fixed))]
 
 
+def sample_key_rows(N: int, P: int, count: int, seed: int):
+    """Seeded key positions (natural order) for element-by-element dK/dV checks.
+
+    Always includes the first keys (seen by every query), the last keys (seen
+    by few), both sides of every chunk boundary of the contiguous (N/P) and
+    folded (N/(2P)) partitions and of every 32768-row block, and the rest
+    uniform over [0, N) without repeats."""
+    fixed = {0, 1, 2, 127, 128, N - 129, N - 128, N - 2, N - 1}
+    for step in (N // P, N // (2 * P), 32768):
+        if step > 0:
+            for c in range(step, N, step):
+                fixed |= {c - 1, c}
+    fixed = {x for x in fixed if 0 <= x < N}
+    g = torch.Generator().manual_seed(seed)
+    rest = [x for x in torch.randperm(N, generator=g).tolist() if x not in fixed]
+    return sorted(fixed | set(rest[:max(0, count - len(fixed))]))
+
+
 def random_partials(k: int, rows: int, d: int, seed: int, neg_inf_frac: float = 0.0):
     """fp32 partial (O, LSE) pairs for merge tests: O ~ N(0,1), LSE ~ 4 N(0,1);
     a fraction of (partial, row) entries is set to (0, -inf) (a chunk pair in

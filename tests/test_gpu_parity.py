@@ -5,6 +5,7 @@ the value for the bf16 output), LSE max-abs <= 2e-3, dQ/dK/dV relative
 Frobenius error <= 2e-2; permutes bit-exact.
 """
 import os
+import time
 
 import numpy as np
 import pytest
@@ -12,7 +13,8 @@ import torch
 
 from long_context_flashattention_gb300 import dfa
 from long_context_flashattention_gb300.inputs import (WORKLOADS, make_qkvdo, make_workload,
-                                                      random_partials, sample_rows)
+                                                      random_partials, sample_key_rows,
+                                                      sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -326,14 +328,17 @@ def _run_large(orc, wname, kind, nsample=4096):
     ws = dfa.new_workspace(desc, dfa.OP_BWD)
     o, lse = dfa.attn_fwd(*perm[:3], P=P, partition=kind, ws=ws)
     gq, gk, gv = dfa.attn_bwd(*perm[:3], o, perm[3], lse, P=P, partition=kind, ws=ws)
+    # the same forward with an fp32 output, checked at the flat bound beside the bf16 one
+    o32, _ = dfa.attn_fwd(*perm[:3], P=P, partition=kind, ws=ws, o_fp32=True)
     _status(ws)
     del perm
+    o32 = dfa.permute(o32, P, kind, inverse=True)
     o = dfa.permute(o, P, kind, inverse=True)
     lse = dfa.permute(lse, P, kind, inverse=True)
     gq = dfa.permute(gq, P, kind, inverse=True)
     gk = dfa.permute(gk, P, kind, inverse=True)
     gv = dfa.permute(gv, P, kind, inverse=True)
-    _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample)
+    _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample, o32=o32)
 
 
 def _run_large_chunked(orc, w, q, k, v, do, qg, kg, vg, dog, nsample):
@@ -365,9 +370,10 @@ def _run_large_chunked(orc, w, q, k, v, do, qg, kg, vg, dog, nsample):
             dfa.lse_merge(part_o.reshape(1, -1, d), part_l.reshape(1, -1), out_fp32=True,
                           o_out=acc_o, lse_out=acc_l, accumulate=True)
         finals.append((acc_o.reshape(w.B, w.Hq, n, d).to(torch.bfloat16), acc_l.reshape(
-            w.B, w.Hq, n)))
+            w.B, w.Hq, n), acc_o.reshape(w.B, w.Hq, n, d)))
     o = torch.cat([f[0] for f in finals], dim=2)
     lse = torch.cat([f[1] for f in finals], dim=2)
+    o32 = torch.cat([f[2] for f in finals], dim=2)
     gq = torch.zeros(w.B, w.Hq, w.N, d, dtype=torch.float32, device="cuda")
     gk = torch.zeros(w.B, w.Hkv, w.N, d, dtype=torch.float32, device="cuda")
     gv = torch.zeros_like(gk)
@@ -387,24 +393,58 @@ def _run_large_chunked(orc, w, q, k, v, do, qg, kg, vg, dog, nsample):
     torch.cuda.synchronize()
     inv = lambda t: dfa.permute(t.contiguous(), P, kind, inverse=True)
     _check_large(orc, w, q, k, v, do, inv(o), inv(lse), inv(gq.to(torch.bfloat16)),
-                 inv(gk.to(torch.bfloat16)), inv(gv.to(torch.bfloat16)), nsample)
+                 inv(gk.to(torch.bfloat16)), inv(gv.to(torch.bfloat16)), nsample, o32=inv(o32))
 
 
-def _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample):
+# Oracle dK/dV of sampled key rows, per workload: the two 128K partitions run
+# on the same inputs, so the (costly) fp64 statistics are computed once.
+_KV_ORACLE = {}
+KV_ROWS = 4096
+
+
+def _kv_oracle(orc, w, q, k, v, do):
+    if w.name not in _KV_ORACLE:
+        g = np.random.default_rng(w.seed + 1001)
+        b, hk = int(g.integers(w.B)), int(g.integers(w.Hkv))
+        krows = np.array(sample_key_rows(w.N, w.P, KV_ROWS, seed=w.seed + 1002))
+        t0 = time.perf_counter()
+        dkr, dvr = orc.attn_bwd_kv_rows(q, k, v, do, b, hk, krows)
+        secs = time.perf_counter() - t0
+        print(f"\n[{w.name}] oracle dK/dV of {len(krows)} key rows of group (b={b}, "
+              f"h_kv={hk}): {secs:.1f} s on {orc.num_threads()} threads", flush=True)
+        _KV_ORACLE[w.name] = (b, hk, krows, dkr, dvr)
+    return _KV_ORACLE[w.name]
+
+
+def _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample, o32=None):
     torch.cuda.synchronize()
     rows = np.array(sample_rows(w.B, w.Hq, w.N, nsample, seed=w.seed + 1000, chunk=w.N // w.P))
+    ridx = torch.from_numpy(rows).cuda()
     ro, rl = orc.attn_fwd(q, k, v, rows=rows)
-    check_o(o.reshape(-1, w.d)[torch.from_numpy(rows).cuda()], ro)
-    check_lse(lse.reshape(-1)[torch.from_numpy(rows).cuda()], rl)
+    check_o(o.reshape(-1, w.d)[ridx], ro)
+    if o32 is not None:   # fp32 output: the flat 1e-2 bound, no half-ulp allowance
+        assert o32.dtype == torch.float32
+        check_o(o32.reshape(-1, w.d)[ridx], ro, "O (fp32 output)")
+    check_lse(lse.reshape(-1)[ridx], rl)
     dqr, _, _ = orc.attn_bwd_q_rows(q, k, v, do, rows)
-    check_grad(gq.reshape(-1, w.d)[torch.from_numpy(rows).cuda()], dqr, "dQ rows")
-    # exact dK/dV for the last key rows of one group (few queries see them)
-    krows = np.arange(w.N - 128, w.N)
-    dkr, dvr = orc.attn_bwd_kv_rows(q, k, v, do, 0, w.Hkv - 1, krows)
-    kidx = torch.from_numpy(krows).cuda()
-    check_grad(gk[0, w.Hkv - 1][kidx], dkr, "dK rows")
-    check_grad(gv[0, w.Hkv - 1][kidx], dvr, "dV rows")
-    # invariants over every key row of every head
+    check_grad(gq.reshape(-1, w.d)[ridx], dqr, "dQ rows")
+    # dK/dV element by element on sampled key rows of one seeded (b, kv-head)
+    # group, spread over the whole sequence: the first keys (seen by every
+    # query, summed over every query block and ring step), chunk and block
+    # boundaries, and the last keys
+    if w.N <= 131072 or os.environ.get("DFA_512K_KV") == "1":
+        b, hk, krows, dkr, dvr = _kv_oracle(orc, w, q, k, v, do)
+        kidx = torch.from_numpy(krows).cuda()
+        check_grad(gk[b, hk][kidx], dkr, "dK rows")
+        check_grad(gv[b, hk][kidx], dvr, "dV rows")
+    else:
+        # 512K without DFA_512K_KV=1: exact dK/dV for the last key rows only
+        krows = np.arange(w.N - 128, w.N)
+        dkr, dvr = orc.attn_bwd_kv_rows(q, k, v, do, 0, w.Hkv - 1, krows)
+        kidx = torch.from_numpy(krows).cuda()
+        check_grad(gk[0, w.Hkv - 1][kidx], dkr, "dK rows")
+        check_grad(gv[0, w.Hkv - 1][kidx], dvr, "dV rows")
+    # invariants over every key row of every head (extras beside the rows above)
     G = w.Hq // w.Hkv
     dof = do.float().cuda()
     sum_do = dof.reshape(w.B, w.Hkv, G, w.N, w.d).sum(dim=(2, 3)).double()
