@@ -11,15 +11,19 @@
 //
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes: every
 // GPU that loads the library holds it until the process exits.  Its device
-// address is looked up once per device (cudaGetSymbolAddress, with that
-// device current) on the first call made on that device; that first call
-// should therefore come before any stream capture.  Every call on a device
-// shares the one array, which keeps the last call's contents: calls that
-// overlap on the GPU (different streams, no ordering between them) race on it.
+// address is looked up once per device context (cudaGetSymbolAddress, with
+// that device current) on the first call made in that context; that first
+// call should therefore come before any stream capture.  A context that ends
+// (cudaDeviceReset) takes the array with it: the next call, in the new
+// context, looks the address up again, because the cache is keyed on the
+// context's unique id.  Every call on a device shares the one array, which
+// keeps the last call's contents: calls that overlap on the GPU (different
+// streams, no ordering between them) race on it.
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/dfa.h"
@@ -40,6 +44,40 @@ constexpr size_t kStatusBytes = 256;
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if it cannot be read),
+// through the driver entry points the runtime exposes.
+unsigned long long current_context_id()
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = (CtxGetCurrentFn)a;
+            get_id = (CtxGetIdFn)b;
+        }
+        looked_up = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
 
 }  // namespace
 
@@ -48,11 +86,16 @@ extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void
                                            const void* dout, const float* lse, void* dq,
                                            void* dk, void* dv, void* stream)
 {
-    if (!desc)
-        return dfa::set_error(DFA_ERR_INVALID_ARG, "desc is NULL");
+    // Argument errors first, with no work queued: dfa_attn_bwd checks the
+    // descriptor and the pointers before the workspace, so without one it
+    // returns DFA_ERR_WORKSPACE exactly when everything else is valid.
+    const dfa_status pre =
+        dfa_attn_bwd(desc, q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, stream);
+    if (pre != DFA_ERR_WORKSPACE)
+        return pre;
     // scratch this problem needs: the workspace of dfa_attn_bwd (status word,
     // fp32 dQ accumulator, per-row records, and with query blocking fp32 dK
-    // and dV); an invalid descriptor is left to dfa_attn_bwd to report
+    // and dV)
     const size_t need = dfa_workspace_size(desc, DFA_OP_BWD);
     if (need > kNoAllocScratchBytes)
         return dfa::set_error(DFA_ERR_WORKSPACE,
@@ -64,13 +107,15 @@ extern "C" dfa_status dfa_attn_bwd_noalloc(const dfa_attn_desc* desc, const void
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!g_scratch_ptr[dev]) {
+        const unsigned long long ctx = current_context_id();
+        if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
             void* ptr = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
             if (e != cudaSuccess || !ptr)
                 return dfa::set_error(DFA_ERR_CUDA, "dfa_attn_bwd_noalloc: scratch lookup: %s",
                                       cudaGetErrorString(e));
             g_scratch_ptr[dev] = ptr;
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_ptr[dev];
     }

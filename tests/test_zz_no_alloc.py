@@ -25,9 +25,15 @@ def _rel(a, b):
 
 
 @pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
-def test_noalloc_backward_matches_workspace_backward_twice():
+@pytest.mark.parametrize("shape", [(1, 4, 2, 1024, 128), (1, 1, 1, 70000, 64)])
+def test_noalloc_backward_matches_workspace_backward_twice(shape):
+    """Two shapes: a small grouped-query problem, and 70000 rows of one head,
+    above the 65536 rows at which the backward sums dK/dV over blocks of
+    query rows in fp32 accumulators -- which then also live in the fixed
+    array (about 58 MB of its 64 MiB)."""
     L = dfa.lib()
-    q, k, v, do = (t.cuda() for t in make_qkvdo(1, 4, 2, 1024, 128, seed=21))
+    B, Hq, Hkv, N, d = shape
+    q, k, v, do = (t.cuda() for t in make_qkvdo(B, Hq, Hkv, N, d, seed=21))
     desc = dfa.desc_for(q, k)
     ws = dfa.new_workspace(desc, dfa.OP_BWD)
     o, lse = dfa.attn_fwd(q, k, v, ws=ws)
@@ -53,3 +59,15 @@ def test_noalloc_rejects_problems_above_its_scratch():
     code = L.dfa_attn_bwd_noalloc(ctypes.byref(desc), p, p, p, p, p, p, p, p, p, None)
     assert code == 3
     assert b"scratch" in L.dfa_last_error()
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="no CUDA device")
+def test_noalloc_reports_argument_errors_before_any_work():
+    L = dfa.lib()
+    desc = dfa.make_desc(1, 1, 1, 256, 96)          # head dimension 96: unsupported
+    p = ctypes.c_void_p(16)
+    assert L.dfa_attn_bwd_noalloc(ctypes.byref(desc), p, p, p, p, p, p, p, p, p, None) == 2
+    desc = dfa.make_desc(1, 1, 1, 256, 64)
+    args = [p] * 9
+    args[3] = None                                  # o is NULL
+    assert L.dfa_attn_bwd_noalloc(ctypes.byref(desc), *args, None) == 1
