@@ -189,19 +189,34 @@ extern "C" size_t dfa_attn_step_host_workspace_size(const dfa_attn_desc* desc,
     return make_plan(desc, kv_heads_per_group, pl) == DFA_OK ? pl.total : 0;
 }
 
-extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* h_q,
-                                         const void* h_k, const void* h_v, const void* h_dout,
-                                         void* h_o, float* h_lse, void* h_dq, void* h_dk,
-                                         void* h_dv, int32_t kv_heads_per_group, void* ws,
-                                         size_t ws_bytes, void* compute_stream,
-                                         void* h2d_stream, void* d2h_stream)
+namespace {
+
+// Host tensors of one step.
+struct HostStep {
+    const void *q, *k, *v, *dout;
+    void *o, *dq, *dk, *dv;
+    float* lse;
+};
+
+// nsteps steps as one stream of (step, group) items: item i is group
+// i % groups of step i / groups, so the uploads of a step's first groups
+// overlap the compute of the previous step's last groups.
+dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* hs,
+                     int32_t kv_heads_per_group, void* ws, size_t ws_bytes, void* compute_stream,
+                     void* h2d_stream, void* d2h_stream)
 {
     Plan pl;
     dfa_status st = make_plan(desc, kv_heads_per_group, pl);
     if (st != DFA_OK)
         return st;
-    if (!h_q || !h_k || !h_v || !h_dout || !h_o || !h_lse || !h_dq || !h_dk || !h_dv)
-        return dfa::set_error(DFA_ERR_INVALID_ARG, "dfa_attn_step_host: a host pointer is NULL");
+    if (nsteps < 1 || !hs)
+        return dfa::set_error(DFA_ERR_INVALID_ARG, "dfa_attn_step_host: need nsteps >= 1");
+    for (int32_t t = 0; t < nsteps; ++t) {
+        const HostStep& h = hs[t];
+        if (!h.q || !h.k || !h.v || !h.dout || !h.o || !h.lse || !h.dq || !h.dk || !h.dv)
+            return dfa::set_error(DFA_ERR_INVALID_ARG,
+                                  "dfa_attn_step_host: a host pointer of step %d is NULL", t);
+    }
     if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < pl.total)
         return dfa::set_error(DFA_ERR_WORKSPACE, "dfa_attn_step_host: workspace must be "
                               "256-byte aligned and hold %zu bytes", pl.total);
@@ -226,54 +241,57 @@ extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* 
     const int r = desc->Hq / desc->Hkv;
     const int64_t heads_q = pl.gd.Hq, heads_k = pl.gk;
     const int64_t d = desc->d;
+    const int64_t items = (int64_t)nsteps * pl.groups;
     auto host_off_q = [&](int g) {  // element offset of group g in a [B,Hq,N,d] tensor
         return ((int64_t)(g / per_b) * desc->Hq + (int64_t)(g % per_b) * pl.gk * r) * desc->N;
     };
     auto host_off_k = [&](int g) {
         return ((int64_t)(g / per_b) * desc->Hkv + (int64_t)(g % per_b) * pl.gk) * desc->N;
     };
-    auto upload = [&](int g) -> cudaError_t {
-        const int s = g % 2;
+    auto upload = [&](int64_t i) -> cudaError_t {
+        const int s = (int)(i % 2), g = (int)(i % pl.groups);
+        const HostStep& h = hs[i / pl.groups];
         const InSet in = in_set(base + pl.off_in[s], pl);
         const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
         cudaError_t x = cudaSuccess;
-        if (g >= 2)
+        if (i >= 2)
             x = cudaStreamWaitEvent(up, ev.e[Events::kInFree0 + s], 0);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.q, (const char*)h_q + oq, pl.qb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.q, (const char*)h.q + oq, pl.qb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.k, (const char*)h_k + ok, pl.kb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.k, (const char*)h.k + ok, pl.kb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.v, (const char*)h_v + ok, pl.kb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.v, (const char*)h.v + ok, pl.kb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.dout, (const char*)h_dout + oq, pl.qb, cudaMemcpyHostToDevice,
+            x = cudaMemcpyAsync(in.dout, (const char*)h.dout + oq, pl.qb, cudaMemcpyHostToDevice,
                                 up);
         if (x == cudaSuccess)
             x = cudaEventRecord(ev.e[Events::kUp0 + s], up);
         return x;
     };
-    auto download = [&](int g) -> cudaError_t {
-        const int s = g % 2;
+    auto download = [&](int64_t i) -> cudaError_t {
+        const int s = (int)(i % 2), g = (int)(i % pl.groups);
+        const HostStep& h = hs[i / pl.groups];
         const OutSet out = out_set(base + pl.off_out[s], pl);
         const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
         const int64_t ol = host_off_q(g) * 4;
         cudaError_t x = cudaStreamWaitEvent(dn, ev.e[Events::kDone], 0);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h_o + oq, out.o, pl.qb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.o + oq, out.o, pl.qb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h_lse + ol, out.lse, pl.lb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.lse + ol, out.lse, pl.lb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h_dq + oq, out.dq, pl.qb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dq + oq, out.dq, pl.qb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h_dk + ok, out.dk, pl.kb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dk + ok, out.dk, pl.kb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h_dv + ok, out.dv, pl.kb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dv + ok, out.dv, pl.kb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
             x = cudaEventRecord(ev.e[Events::kDown0 + s], dn);
         return x;
     };
-    auto compute = [&](int g) -> dfa_status {
-        const int s = g % 2;
+    auto compute = [&](int64_t i) -> dfa_status {
+        const int s = (int)(i % 2);
         const InSet in = in_set(base + pl.off_in[s], pl);
         const OutSet out = out_set(base + pl.off_out[s], pl);
         const InSet pin = pl.ident ? in : in_set(base + pl.off_pin, pl);
@@ -296,8 +314,8 @@ extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* 
             if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
                 return cuda_err(x, "event record");
         }
-        // the output slot was last read by the download of group g - 2
-        if (pl.ident && g >= 2 && dn != cs &&
+        // the output slot was last read by the download of item i - 2
+        if (pl.ident && i >= 2 && dn != cs &&
             (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
             return cuda_err(x, "stream wait");
         t = dfa_attn_fwd(gd, pin.q, pin.k, pin.v, pout.o, (float*)pout.lse, ws, 256, cs);
@@ -310,7 +328,7 @@ extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* 
             if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
                 return cuda_err(x, "event record");
         } else {
-            if (g >= 2 && dn != cs &&
+            if (i >= 2 && dn != cs &&
                 (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
                 return cuda_err(x, "stream wait");
             t = dfa_permute(gd, 1, pout.o, out.o, 2, d, heads_q, cs);
@@ -330,19 +348,19 @@ extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* 
         return DFA_OK;
     };
 
-    // Issue order: the next group's upload goes into its queue before this
-    // group's compute, so the copy engine never waits on the host.
+    // Issue order: the next item's upload goes into its queue before this
+    // item's compute, so the copy engine never waits on the host.
     e = upload(0);
     if (e != cudaSuccess)
         st = cuda_err(e, "upload");
-    for (int g = 0; g < pl.groups && st == DFA_OK; ++g) {
-        if (g + 1 < pl.groups && (e = upload(g + 1)) != cudaSuccess) {
+    for (int64_t i = 0; i < items && st == DFA_OK; ++i) {
+        if (i + 1 < items && (e = upload(i + 1)) != cudaSuccess) {
             st = cuda_err(e, "upload");
             break;
         }
-        if ((st = compute(g)) != DFA_OK)
+        if ((st = compute(i)) != DFA_OK)
             break;
-        if ((e = download(g)) != cudaSuccess)
+        if ((e = download(i)) != cudaSuccess)
             st = cuda_err(e, "download");
     }
     // Join: everything queued on the copy streams is ordered before later
@@ -361,4 +379,39 @@ extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* 
     if (st == DFA_OK && j != cudaSuccess)
         st = cuda_err(j, "join");
     return st;
+}
+
+}  // namespace
+
+extern "C" dfa_status dfa_attn_step_host(const dfa_attn_desc* desc, const void* h_q,
+                                         const void* h_k, const void* h_v, const void* h_dout,
+                                         void* h_o, float* h_lse, void* h_dq, void* h_dk,
+                                         void* h_dv, int32_t kv_heads_per_group, void* ws,
+                                         size_t ws_bytes, void* compute_stream,
+                                         void* h2d_stream, void* d2h_stream)
+{
+    const HostStep h{h_q, h_k, h_v, h_dout, h_o, h_dq, h_dk, h_dv, h_lse};
+    return run_steps(desc, 1, &h, kv_heads_per_group, ws, ws_bytes, compute_stream, h2d_stream,
+                     d2h_stream);
+}
+
+extern "C" dfa_status dfa_attn_steps_host(const dfa_attn_desc* desc, int32_t nsteps,
+                                          const dfa_host_step* steps, int32_t kv_heads_per_group,
+                                          void* ws, size_t ws_bytes, void* compute_stream,
+                                          void* h2d_stream, void* d2h_stream)
+{
+    if (nsteps < 1 || !steps)
+        return dfa::set_error(DFA_ERR_INVALID_ARG, "dfa_attn_steps_host: need nsteps >= 1 and "
+                              "a step array");
+    // dfa_host_step and HostStep hold the same pointers; copy field by field
+    constexpr int32_t kChunk = 64;
+    HostStep hs[kChunk];
+    if (nsteps > kChunk)
+        return dfa::set_error(DFA_ERR_UNSUPPORTED, "dfa_attn_steps_host: at most %d steps per "
+                              "call", kChunk);
+    for (int32_t t = 0; t < nsteps; ++t)
+        hs[t] = HostStep{steps[t].q, steps[t].k, steps[t].v, steps[t].dout, steps[t].o,
+                         steps[t].dq, steps[t].dk, steps[t].dv, steps[t].lse};
+    return run_steps(desc, nsteps, hs, kv_heads_per_group, ws, ws_bytes, compute_stream,
+                     h2d_stream, d2h_stream);
 }

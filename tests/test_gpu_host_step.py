@@ -107,3 +107,19 @@ def test_step_host_reuses_workspace_and_outputs():
     for a, b in zip(first[2:], again[2:]):
         assert float((a.float() - b.float()).norm() / b.float().norm()) <= 2e-3
         assert np.isfinite(b.float().numpy()).all()
+
+
+def test_steps_host_equals_single_steps():
+    """Three steps in one dfa_attn_steps_host call (items of consecutive steps
+    overlap) give what three dfa_attn_step_host calls give: O and LSE bit for
+    bit, gradients to fp32 atomic-order noise; the steps have different
+    inputs, so a mix-up of steps would show."""
+    B, Hq, Hkv, N, d, P, kind = 1, 4, 2, 2048, 128, 2, "balanced"
+    steps = [_pinned(*make_qkvdo(B, Hq, Hkv, N, d, seed=200 + t)) for t in range(3)]
+    multi = dfa.attn_steps_host(steps, P=P, partition=kind, kv_heads_per_group=1)
+    torch.cuda.synchronize()
+    for st, got in zip(steps, multi):
+        ref = _step_host(*st, P=P, partition=kind, kv_heads_per_group=1)
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+        for a, b in zip(got[2:], ref[2:]):
+            assert float((a.float() - b.float()).norm() / b.float().norm()) <= 2e-3
