@@ -302,12 +302,14 @@ dfa_status check_ws(void* ws, size_t have, size_t need)
 // Above this many query rows per head the backward cuts the query side into
 // blocks of about kBwdBlockRows rows (same local tile range in every query
 // chunk): the units running at one time then share one block's Q, dO and dQ
-// rows (about 32 MB) in L2 instead of a whole head's, and dK / dV are summed
-// over the blocks in fp32.  The count is per head, not per key/value group:
-// measured on grouped-query attention (4 query heads per key/value head, 64K
-// rows), blocks of 8K rows per head ran the backward slower than no blocks,
-// the running units then streaming the group's rows in near lockstep.
-constexpr int64_t kBwdBlockAbove = 65536, kBwdBlockRows = 32768;
+// rows in L2 instead of a whole head's (or a whole grouped-query head
+// group's), and dK / dV are summed over the blocks in fp32.  Measured on
+// GB300: grouped-query attention (4 query heads per key/value head, 64K rows)
+// 840 -> 888 TFLOP/s with blocks of 32K rows per head; smaller blocks are
+// slower (16K: 844, 8K: 722; and at 128K rows, 16K blocks 886 against 987
+// for 32K), the units then being shorter while each still pays its K/V load
+// and its fp32 dK/dV sums.
+constexpr int64_t kBwdBlockAbove = 32768, kBwdBlockRows = 32768;
 
 bool bwd_blocked(int64_t q_rows_per_head) { return q_rows_per_head > kBwdBlockAbove; }
 

@@ -466,6 +466,7 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
     const uint32_t tl = sh.tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t tS = tl + C::cS + 64 * h, tDP = tl + C::cDP + 64 * h;
     uint8_t* dsb = sh.smem + C::kDs + h * 16384;
+    const uint32_t dsb_s = smem_u32(dsb);
     const uint64_t c2x2 = f2pack(p.scale_log2, p.scale_log2);
     uint32_t n = 0, uc = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -543,9 +544,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                             tmem_st16(tDP + 16 * c, dd);
 #pragma unroll
                             for (int ch = 0; ch < 4; ++ch)
-                                *(uint4*)(dsb + sw128_offset(r, 4 * c + ch)) =
-                                    make_uint4(dd[4 * ch], dd[4 * ch + 1], dd[4 * ch + 2],
-                                               dd[4 * ch + 3]);
+                                st_shared_v4(dsb_s + sw128_offset(r, 4 * c + ch), dd[4 * ch],
+                                             dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
                         }
                         tmem_st_wait();
                         fence_proxy_async_smem();
@@ -602,11 +602,11 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                 float* stage = reinterpret_cast<float*>(dsb);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    *reinterpret_cast<float4*>(stage + r * 32 + ((e ^ (r & 7)) * 4)) =
-                        make_float4(__uint_as_float(o[4 * e + 0]) * mul,
-                                    __uint_as_float(o[4 * e + 1]) * mul,
-                                    __uint_as_float(o[4 * e + 2]) * mul,
-                                    __uint_as_float(o[4 * e + 3]) * mul);
+                    st_shared_v4(dsb_s + sw128_offset(r, e),
+                                 __float_as_uint(__uint_as_float(o[4 * e + 0]) * mul),
+                                 __float_as_uint(__uint_as_float(o[4 * e + 1]) * mul),
+                                 __float_as_uint(__uint_as_float(o[4 * e + 2]) * mul),
+                                 __float_as_uint(__uint_as_float(o[4 * e + 3]) * mul));
                 asm volatile("bar.sync %0, 128;" ::"r"(1 + h) : "memory");
                 const int wq = warp & 3;
                 const size_t rbase = (size_t)un.slice * p.Lk + (size_t)un.chunk * p.chunk_k + un.row0;

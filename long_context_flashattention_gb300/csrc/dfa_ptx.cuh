@@ -482,6 +482,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
+// One 16-byte shared-memory store (a single 128-bit access, so that eight
+// lanes writing distinct 16-byte columns of a swizzled tile make one
+// conflict-free wavefront).
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 // 128-byte swizzle: byte offset of 16-byte chunk `c` (0..7) of row `r` inside
 // a 1024-byte aligned tile whose rows are 128 bytes.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c)

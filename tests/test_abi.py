@@ -34,7 +34,7 @@ def test_workspace_sizes():
     d = dfa.make_desc(1, 32, 32, 131072, 128, P=8, partition="striped")
     assert dfa.workspace_size(d, dfa.OP_FWD) == 256
     # status word, fp32 dQ accumulator, 32-byte -LSE/scale and -D records per row,
-    # and (query blocking above 64K rows per head) fp32 dK and dV
+    # and (query blocking above 32K rows per head) fp32 dK and dV
     need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32 + 2 * 32 * 131072 * 128 * 4
     assert dfa.workspace_size(d, dfa.OP_BWD) == need
     assert dfa.workspace_size(d, dfa.OP_CHUNK_BWD) == 256 + 2 * 32 * 131072 * 32
@@ -44,6 +44,11 @@ def test_workspace_sizes():
     g = dfa.make_desc(1, 2, 1, 65600, 64)
     assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 2 * 65600 * 64 * 4 + 2 * 2 * 65600 * 32
                                                  + 2 * 65600 * 64 * 4)
+    g = dfa.make_desc(1, 2, 1, 32768, 64)   # exactly 32K rows per head: not blocked
+    assert dfa.workspace_size(g, dfa.OP_BWD) == 256 + 2 * 32768 * 64 * 4 + 2 * 2 * 32768 * 32
+    g = dfa.make_desc(1, 2, 1, 32896, 64)   # above: fp32 dK and dV too
+    assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 2 * 32896 * 64 * 4 + 2 * 2 * 32896 * 32
+                                                 + 2 * 32896 * 64 * 4)
     bad = dfa.make_desc(1, 32, 32, 1000, 128, P=3)
     assert dfa.workspace_size(bad, dfa.OP_FWD) == 0
 

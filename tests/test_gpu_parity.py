@@ -461,7 +461,7 @@ def _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample, o32=None):
 
 
 def test_query_blocked_backward_ragged(orc):
-    """Above 64K query rows per head the backward cuts the queries into blocks
+    """Above 32K query rows per head the backward cuts the queries into blocks
     and sums dK/dV over them in fp32.  N = 70000 gives blocks [0, 32768),
     [32768, 65536), [65536, 70000); the key rows checked exactly straddle the
     last boundary, so their gradients are sums over two blocks."""
@@ -491,7 +491,7 @@ def test_query_blocked_backward_ragged(orc):
 
 def test_query_blocked_backward_gqa_striped(orc):
     """Query blocking with grouped-query heads (G = 2) on a striped partition:
-    N = 66048 > 65536 rows per head gives blocks of 32768 / 4 = 8192 rows per
+    N = 66048 > 32768 rows per head gives blocks of 32768 / 4 = 8192 rows per
     chunk (P = 4); the key rows checked straddle position 65536, so their
     dK/dV sum over two blocks and both query heads of the group."""
     B, Hq, Hkv, N, d, P, kind = 1, 2, 1, 66048, 64, 4, "striped"

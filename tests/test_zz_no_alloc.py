@@ -28,7 +28,7 @@ def _rel(a, b):
 @pytest.mark.parametrize("shape", [(1, 4, 2, 1024, 128), (1, 1, 1, 70000, 64)])
 def test_noalloc_backward_matches_workspace_backward_twice(shape):
     """Two shapes: a small grouped-query problem, and 70000 rows of one head,
-    above the 65536 rows at which the backward sums dK/dV over blocks of
+    above the 32768 rows at which the backward sums dK/dV over blocks of
     query rows in fp32 accumulators -- which then also live in the fixed
     array (about 58 MB of its 64 MiB)."""
     L = dfa.lib()
