@@ -275,7 +275,9 @@ dfa_status dfa_ring_fwd(const dfa_attn_desc* desc, const dfa_ring_worker* worker
  *   log-sum-exp).  Host buffers must stay valid and untouched until
  *   compute_stream has passed the call's work.
  *   kv_heads_per_group: a divisor of Hkv, or 0 for the library's choice
- *   (at least 8 groups where B*Hkv allows).
+ *   (the fewest heads per group that still give the group's backward at
+ *   least 2432 key tiles of 128 rows, and at least two groups where B*Hkv
+ *   allows).
  *   ws: dfa_attn_step_host_workspace_size(desc, kv_heads_per_group) bytes,
  *   status word first (dfa_stream_status reads the backward's timeouts).
  * desc->o_fp32 must be 0 (DFA_ERR_UNSUPPORTED otherwise).  When the call

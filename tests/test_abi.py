@@ -246,9 +246,18 @@ def test_step_host_workspace_layout():
     d1 = dfa.make_desc(1, 4, 4, 4096, 64, P=4, partition="striped", stripe=1024)
     d2 = dfa.make_desc(1, 4, 4, 4096, 64, P=4, partition="contiguous")
     assert _step_host_ws(d1, 1) == _step_host_ws(d2, 1)
-    # fewer than 8 key/value heads in all: one head per group
+    # the automatic group: the fewest heads whose backward has >= 2432 key
+    # tiles of 128 rows, at least two groups: 16 heads at 32K (two groups)...
+    d32 = dfa.make_desc(1, 32, 32, 32768, 128, P=8, partition="balanced")
+    assert _step_host_ws(d32, 0) == _step_host_ws(d32, 16)
+    # ...one head per group at 512K...
+    d512 = dfa.make_desc(1, 32, 32, 524288, 128, P=16, partition="balanced")
+    assert _step_host_ws(d512, 0) == _step_host_ws(d512, 1)
+    # ...and a problem too small for the rule still gets two groups
     small = dfa.make_desc(2, 4, 2, 1024, 128)
-    assert _step_host_ws(small, 0) == _step_host_ws(small, 1)
+    assert _step_host_ws(small, 0) == _step_host_ws(small, 2)
+    one = dfa.make_desc(1, 4, 2, 1024, 128)
+    assert _step_host_ws(one, 0) == _step_host_ws(one, 1)
 
 
 def test_step_host_validation(L):
