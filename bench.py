@@ -208,7 +208,7 @@ def run_gpu(args):
     # permutes in, forward, backward (preprocess, main kernel, dQ conversion;
     # with query blocking above 64K rows per head also dK and dV conversions),
     # permutes out
-    blocked = w.N > 32768
+    blocked = w.N * (w.Hq // w.Hkv) > 131072
     launches_per_step = 4 + 1 + (5 if blocked else 3) + 5
 
     def barrier():

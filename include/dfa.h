@@ -159,7 +159,8 @@ dfa_status dfa_attn_fwd(const dfa_attn_desc* desc, const void* q, const void* k,
  *   lse [B,Hq,N] fp32 (the forward's);  dq [B,Hq,N,d], dk/dv [B,Hkv,N,d] bf16.
  *   ws: dfa_workspace_size(desc, DFA_OP_BWD) bytes: the fp32 dQ accumulator
  *   and, per query row, 32-byte records of -LSE/scale and -D that the
- *   kernel adds to S and dP on the tensor core; when N > 32768 also fp32
+ *   kernel adds to S and dP on the tensor core; when N * Hq/Hkv > 131072
+ *   also fp32
  *   dK and dV, which the kernel sums over blocks of query rows before the
  *   bf16 conversion.
  */
@@ -460,7 +461,7 @@ dfa_status dfa_partition_map(const dfa_attn_desc* desc, int32_t p, dfa_pos_map* 
  * a plugin handed buffers by a host framework, a host callback, a loop that
  * forbids cudaMalloc after start-up.  dfa_attn_bwd needs a workspace of
  * dfa_workspace_size(desc, DFA_OP_BWD) bytes (256 + B*Hq*N*(4d + 64),
- * rounded, plus 8*B*Hkv*N*d when N > 32768); here that scratch is
+ * rounded, plus 8*B*Hkv*N*d when N * Hq/Hkv > 131072); here that scratch is
  * a fixed 64 MiB array in device memory owned by the library, held
  * by every GPU that loads the library until the process exits.  Problems
  * whose scratch would exceed 64 MiB are rejected with DFA_ERR_WORKSPACE.

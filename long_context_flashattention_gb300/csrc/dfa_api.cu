@@ -299,19 +299,23 @@ dfa_status check_ws(void* ws, size_t have, size_t need)
 // forward / backward launches over a layout of nq query chunks and nkv kv
 // chunks (shared by the whole-sequence and chunk-pair calls)
 // ----------------------------------------------------------------------------
-// Above this many query rows per head the backward cuts the query side into
-// blocks of about kBwdBlockRows rows (same local tile range in every query
-// chunk): the units running at one time then share one block's Q, dO and dQ
-// rows in L2 instead of a whole head's (or a whole grouped-query head
-// group's), and dK / dV are summed over the blocks in fp32.  Measured on
-// GB300: grouped-query attention (4 query heads per key/value head, 64K rows)
-// 840 -> 888 TFLOP/s with blocks of 32K rows per head; smaller blocks are
-// slower (16K: 844, 8K: 722; and at 128K rows, 16K blocks 886 against 987
-// for 32K), the units then being shorter while each still pays its K/V load
-// and its fp32 dK/dV sums.
-constexpr int64_t kBwdBlockAbove = 32768, kBwdBlockRows = 32768;
+// When a key/value head's query rows -- N rows for each of its G query
+// heads -- exceed kBwdBlockAbove, the backward cuts the query side into
+// blocks (the same local tile range in every query chunk) of
+// max(32768, 65536 / G) rows per head, so that the units running at one time
+// share one block's Q, dO and dQ rows (G x rows x 1 KB, 64-128 MB) in L2;
+// dK and dV are then summed over the blocks in fp32.  Every block pass reads
+// and writes those fp32 sums, so fewer blocks cost less DRAM traffic (and
+// power under the 1.4 kW cap).  Measured on GB300 (backward TFLOP/s):
+// Llama-7B 128K, 32 heads: no blocks 1033 (striped and folded alike),
+// 64K-row blocks 1027 / 994, 32K-row blocks 983 / 906;  512K, 8 heads
+// (folded): 64K blocks 1013, 128K blocks 990, 32K blocks 927;  grouped-query
+// 64K (G = 4): 32K blocks 895, 16K 844, one 64K block 833, none 838.
+constexpr int64_t kBwdBlockAbove = 131072;
 
-bool bwd_blocked(int64_t q_rows_per_head) { return q_rows_per_head > kBwdBlockAbove; }
+bool bwd_blocked(int64_t q_rows_per_head, int G) { return q_rows_per_head * G > kBwdBlockAbove; }
+
+int64_t bwd_block_rows(int G) { return std::max<int64_t>(32768, 65536 / std::max(1, G)); }
 
 struct Layout {
     std::vector<dfa_pos_map> qmaps, kmaps;
@@ -401,9 +405,9 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     const int64_t nqt = (lay.chunk_q + bq - 1) / bq;
     p.nqblk = 1;
     p.qblk_tiles = (int32_t)nqt;
-    if (bwd_blocked(Lq)) {
+    if (bwd_blocked(Lq, d.Hq / d.Hkv)) {
         const int64_t rows_per_chunk =
-            std::max<int64_t>(bq, kBwdBlockRows / (int64_t)lay.qmaps.size());
+            std::max<int64_t>(bq, bwd_block_rows(d.Hq / d.Hkv) / (int64_t)lay.qmaps.size());
         p.qblk_tiles = (int32_t)std::max<int64_t>(1, rows_per_chunk / bq);
         p.nqblk = (int32_t)((nqt + p.qblk_tiles - 1) / p.qblk_tiles);
     }
@@ -480,7 +484,7 @@ size_t bwd_ws_bytes(const dfa_attn_desc& d)
     const size_t rows = (size_t)d.B * d.Hq * (size_t)d.N;
     const size_t kv = (size_t)d.B * d.Hkv * (size_t)d.N * d.d * 4;
     return kStatusBytes + align256(rows * d.d * 4) + 2 * align256(rows * kAugRowBytes) +
-           (bwd_blocked(d.N) ? 2 * align256(kv) : 0);
+           (bwd_blocked(d.N, d.Hq / d.Hkv) ? 2 * align256(kv) : 0);
 }
 
 }  // namespace
@@ -628,7 +632,7 @@ dfa_status dfa_attn_bwd(const dfa_attn_desc* desc, const void* q, const void* k,
                                           aug_lse, aug_delta, dq_acc, sms, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward preprocess launch");
-    const bool blocked = bwd_blocked(desc->N);
+    const bool blocked = bwd_blocked(desc->N, desc->Hq / desc->Hkv);
     const int64_t kv_elems = (int64_t)desc->B * desc->Hkv * desc->N * desc->d;
     float* dk_acc = nullptr;
     float* dv_acc = nullptr;

@@ -34,20 +34,25 @@ def test_workspace_sizes():
     d = dfa.make_desc(1, 32, 32, 131072, 128, P=8, partition="striped")
     assert dfa.workspace_size(d, dfa.OP_FWD) == 256
     # status word, fp32 dQ accumulator, 32-byte -LSE/scale and -D records per row,
-    # and (query blocking above 32K rows per head) fp32 dK and dV
-    need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32 + 2 * 32 * 131072 * 128 * 4
+    # and (query blocking when a key/value head's query rows, N x Hq/Hkv,
+    # exceed 131072) fp32 dK and dV
+    need = 256 + 32 * 131072 * 128 * 4 + 2 * 32 * 131072 * 32
     assert dfa.workspace_size(d, dfa.OP_BWD) == need
     assert dfa.workspace_size(d, dfa.OP_CHUNK_BWD) == 256 + 2 * 32 * 131072 * 32
-    # blocking counts query rows per head, whatever the group size
+    d5 = dfa.make_desc(1, 32, 32, 524288, 128, P=16, partition="balanced")
+    need = (256 + 32 * 524288 * 128 * 4 + 2 * 32 * 524288 * 32 +
+            2 * 32 * 524288 * 128 * 4)
+    assert dfa.workspace_size(d5, dfa.OP_BWD) == need
+    # the rule counts the rows of the whole group: G = 8 at 16K rows is 131072
     g = dfa.make_desc(1, 16, 2, 16384, 64)
     assert dfa.workspace_size(g, dfa.OP_BWD) == 256 + 16 * 16384 * 64 * 4 + 2 * 16 * 16384 * 32
     g = dfa.make_desc(1, 2, 1, 65600, 64)
     assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 2 * 65600 * 64 * 4 + 2 * 2 * 65600 * 32
                                                  + 2 * 65600 * 64 * 4)
-    g = dfa.make_desc(1, 2, 1, 32768, 64)   # exactly 32K rows per head: not blocked
-    assert dfa.workspace_size(g, dfa.OP_BWD) == 256 + 2 * 32768 * 64 * 4 + 2 * 2 * 32768 * 32
-    g = dfa.make_desc(1, 2, 1, 32896, 64)   # above: fp32 dK and dV too
-    assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 2 * 32896 * 64 * 4 + 2 * 2 * 32896 * 32
+    g = dfa.make_desc(1, 4, 1, 32768, 64)   # G x N = 131072 exactly: not blocked
+    assert dfa.workspace_size(g, dfa.OP_BWD) == 256 + 4 * 32768 * 64 * 4 + 2 * 4 * 32768 * 32
+    g = dfa.make_desc(1, 4, 1, 32896, 64)   # above: fp32 dK and dV too
+    assert dfa.workspace_size(g, dfa.OP_BWD) == (256 + 4 * 32896 * 64 * 4 + 2 * 4 * 32896 * 32
                                                  + 2 * 32896 * 64 * 4)
     bad = dfa.make_desc(1, 32, 32, 1000, 128, P=3)
     assert dfa.workspace_size(bad, dfa.OP_FWD) == 0

@@ -62,15 +62,15 @@ def test_decode_query_before_cache_end(orc):
 
 def test_decode_long_cache(orc):
     """Llama-7B shape, 128K cached keys, one new token: every head's output
-    against the oracle on two sampled heads (the others through the same code)."""
+    and LSE against the oracle (32 rows of 131072 keys, about 1 GFLOP in
+    fp64)."""
     B, H, L, d = 1, 32, 131072, 128
     gq = torch.Generator(device="cuda").manual_seed(63)
     q = torch.randn(B, H, 1, d, generator=gq, device="cuda").to(torch.bfloat16)
     k = torch.randn(B, H, L, d, generator=gq, device="cuda").to(torch.bfloat16)
     v = torch.randn(B, H, L, d, generator=gq, device="cuda").to(torch.bfloat16)
     o, lse = dfa.decode(q, k, v, split_len=1024)
-    for h in (0, 31):
-        O, LSE = orc.attn_fwd(q[:, h:h + 1].cpu(), k[:, h:h + 1].cpu(), v[:, h:h + 1].cpu(),
-                              causal=True, qpos=np.array([L - 1]), kpos=np.arange(L))
-        check_o(o[:, h:h + 1], O)
-        check_lse(lse[:, h:h + 1], LSE)
+    O, LSE = orc.attn_fwd(q.cpu(), k.cpu(), v.cpu(), causal=True, qpos=np.array([L - 1]),
+                          kpos=np.arange(L))
+    check_o(o, O)
+    check_lse(lse, LSE)

@@ -461,12 +461,13 @@ def _check_large(orc, w, q, k, v, do, o, lse, gq, gk, gv, nsample, o32=None):
 
 
 def test_query_blocked_backward_ragged(orc):
-    """Above 32K query rows per head the backward cuts the queries into blocks
-    and sums dK/dV over them in fp32.  N = 70000 gives blocks [0, 32768),
-    [32768, 65536), [65536, 70000); the key rows checked exactly straddle the
-    last boundary, so their gradients are sums over two blocks."""
+    """When a key/value head's query rows (N x Hq/Hkv) exceed 131072 the
+    backward cuts the queries into blocks and sums dK/dV over them in fp32.
+    Two query heads of N = 70000 give blocks [0, 32768), [32768, 65536),
+    [65536, 70000); the key rows checked exactly straddle the last boundary,
+    so their gradients are sums over two blocks and both query heads."""
     from long_context_flashattention_gb300.inputs import Workload
-    w = Workload("blocked 70000", 1, 1, 1, 70000, 64, 91, 1, ("contiguous",))
+    w = Workload("blocked 70000", 1, 2, 1, 70000, 64, 91, 1, ("contiguous",))
     q, k, v, do = make_qkvdo(w.B, w.Hq, w.Hkv, w.N, w.d, seed=w.seed)
     qg, kg, vg, dog = (t.cuda() for t in (q, k, v, do))
     o, lse = dfa.attn_fwd(qg, kg, vg)
@@ -477,21 +478,21 @@ def test_query_blocked_backward_ragged(orc):
     kidx = torch.from_numpy(krows).cuda()
     check_grad(gk[0, 0][kidx], dkr, "dK rows across blocks")
     check_grad(gv[0, 0][kidx], dvr, "dV rows across blocks")
-    rows = np.array([0, 1, 32767, 32768, 65535, 65536, 69999] +
-                    list(np.random.default_rng(92).integers(0, w.N, 57)))
+    rows = np.array([0, 1, 32767, 32768, 65535, 65536, 69999, w.N + 65536] +
+                    list(np.random.default_rng(92).integers(0, w.Hq * w.N, 56)))
     ro, rl = orc.attn_fwd(q, k, v, rows=rows)
     check_o(o.reshape(-1, w.d)[torch.from_numpy(rows).cuda()], ro)
     check_lse(lse.reshape(-1)[torch.from_numpy(rows).cuda()], rl)
     dqr, _, _ = orc.attn_bwd_q_rows(q, k, v, do, rows)
     check_grad(gq.reshape(-1, w.d)[torch.from_numpy(rows).cuda()], dqr, "dQ rows")
-    sum_do = dog.double().sum(dim=2)
-    assert float((gv.double().sum(dim=2) - sum_do).norm() / sum_do.norm()) <= G_TOL
+    sum_do = dog.double().sum(dim=(1, 2))
+    assert float((gv.double().sum(dim=(1, 2)) - sum_do).norm() / sum_do.norm()) <= G_TOL
     assert float((gk.double().sum(dim=2).abs() / gk.double().abs().sum(dim=2)).max()) <= G_TOL
 
 
 def test_query_blocked_backward_gqa_striped(orc):
     """Query blocking with grouped-query heads (G = 2) on a striped partition:
-    N = 66048 > 32768 rows per head gives blocks of 32768 / 4 = 8192 rows per
+    2 x 66048 > 131072 rows per key/value head gives blocks of 32768 / 4 = 8192 rows per
     chunk (P = 4); the key rows checked straddle position 65536, so their
     dK/dV sum over two blocks and both query heads of the group."""
     B, Hq, Hkv, N, d, P, kind = 1, 2, 1, 66048, 64, 4, "striped"
