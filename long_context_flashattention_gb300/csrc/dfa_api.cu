@@ -301,21 +301,22 @@ dfa_status check_ws(void* ws, size_t have, size_t need)
 // ----------------------------------------------------------------------------
 // When a key/value head's query rows -- N rows for each of its G query
 // heads -- exceed kBwdBlockAbove, the backward cuts the query side into
-// blocks (the same local tile range in every query chunk) of
-// max(32768, 65536 / G) rows per head, so that the units running at one time
-// share one block's Q, dO and dQ rows (G x rows x 1 KB, 64-128 MB) in L2;
+// blocks (the same local tile range in every query chunk) of 65536 / G rows
+// per head (at least 8192), so that the units running at one time share one
+// block's Q, dO and dQ rows of every head of the group (about 64 MB) in L2;
 // dK and dV are then summed over the blocks in fp32.  Every block pass reads
 // and writes those fp32 sums, so fewer blocks cost less DRAM traffic (and
 // power under the 1.4 kW cap).  Measured on GB300 (backward TFLOP/s):
 // Llama-7B 128K, 32 heads: no blocks 1033 (striped and folded alike),
 // 64K-row blocks 1027 / 994, 32K-row blocks 983 / 906;  512K, 8 heads
 // (folded): 64K blocks 1013, 128K blocks 990, 32K blocks 927;  grouped-query
-// 64K (G = 4): 32K blocks 895, 16K 844, one 64K block 833, none 838.
+// 64K (G = 4, query heads innermost in a unit): 16K blocks 922, 32K 889,
+// none 805.
 constexpr int64_t kBwdBlockAbove = 131072;
 
 bool bwd_blocked(int64_t q_rows_per_head, int G) { return q_rows_per_head * G > kBwdBlockAbove; }
 
-int64_t bwd_block_rows(int G) { return std::max<int64_t>(32768, 65536 / std::max(1, G)); }
+int64_t bwd_block_rows(int G) { return std::max<int64_t>(8192, 65536 / std::max(1, G)); }
 
 struct Layout {
     std::vector<dfa_pos_map> qmaps, kmaps;

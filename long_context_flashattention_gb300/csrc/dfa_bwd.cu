@@ -12,7 +12,10 @@
 //
 // GB300 mapping: one persistent CTA per SM, 512 threads = 4 warpgroups.  A
 // work unit is one 128-row key/value tile; it meets every visible 128-row
-// query tile ("step") of every query head of its group.  Key rows sit on TMEM
+// query tile ("step") of every query head of its group, the group's query
+// heads innermost (all of them at one query tile before the next tile), so
+// that the units running at one time work on the same query rows of every
+// head of the group.  Key rows sit on TMEM
 // lanes, so dK and dV accumulate in TMEM for the whole unit.  Every product
 // of a step is an M = 128, N = 128 (or N = d) tcgen05 MMA: the K, V and K^T
 // operands are read from shared memory once per 128 query rows, and no
@@ -247,11 +250,11 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
         if (*sh.abort_flag)
             return;
         ++uc;
-        for (int g = 0; g < p.G; ++g) {
-            const int slice_q = b * p.Hq + hk * p.G + g;
-            for (int s = 0; s < p.nq; ++s) {
-                QRange qr = q_range(p, un, s);
-                for (int i = qr.i0; i < qr.i1; ++i, ++qc) {
+        for (int s = 0; s < p.nq; ++s) {
+            QRange qr = q_range(p, un, s);
+            for (int i = qr.i0; i < qr.i1; ++i) {
+                for (int g = 0; g < p.G; ++g, ++qc) {
+                    const int slice_q = b * p.Hq + hk * p.G + g;
                     const int st = qc % C::kQStages;
                     const uint32_t use = qc / C::kQStages;
                     const int qrow = qr.p * p.chunk_q + i * BQ;
@@ -477,17 +480,17 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
         int32_t dlo, dhi;
         doc_range(p.docs, p.ndocs, pk, dlo, dhi);
         if (T > 0) {
-            for (int g = 0; g < p.G; ++g) {
-                for (int s = 0; s < p.nq; ++s) {
-                    QRange qr = q_range(p, un, s);
-                    if (qr.i0 >= qr.i1)
-                        continue;
-                    // query rows [qv, qe) of chunk qr.p see this key row
-                    const int32_t qv =
-                        !kvalid ? 0x7fffffff
-                                : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);
-                    const int32_t qe = map_count_le(p.qmap[qr.p], dhi - 1);
-                    for (int i = qr.i0; i < qr.i1; ++i, ++n) {
+            for (int s = 0; s < p.nq; ++s) {
+                QRange qr = q_range(p, un, s);
+                if (qr.i0 >= qr.i1)
+                    continue;
+                // query rows [qv, qe) of chunk qr.p see this key row
+                const int32_t qv =
+                    !kvalid ? 0x7fffffff
+                            : map_count_le(p.qmap[qr.p], (p.causal ? pk : dlo) - 1);
+                const int32_t qe = map_count_le(p.qmap[qr.p], dhi - 1);
+                for (int i = qr.i0; i < qr.i1; ++i) {
+                    for (int g = 0; g < p.G; ++g, ++n) {
                         const uint32_t ph = n & 1;
                         // tiles that see every key row take a path without
                         // any mask arithmetic
@@ -647,13 +650,13 @@ __device__ __forceinline__ void dq_drain(const BwdParams& p, const Shared& sh, c
         if (unit_steps(p, un) == 0)
             continue;
         const int b0 = un.slice / p.Hkv, hk = un.slice % p.Hkv;
-        for (int g = 0; g < p.G; ++g) {
-            const int slice_q = b0 * p.Hq + hk * p.G + g;
-            for (int s = 0; s < p.nq; ++s) {
-                QRange qr = q_range(p, un, s);
-                float* base =
-                    p.dq_acc + ((size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q) * D + L;
-                for (int i = qr.i0; i < qr.i1; ++i, ++n) {
+        for (int s = 0; s < p.nq; ++s) {
+            QRange qr = q_range(p, un, s);
+            for (int i = qr.i0; i < qr.i1; ++i) {
+                for (int g = 0; g < p.G; ++g, ++n) {
+                    const int slice_q = b0 * p.Hq + hk * p.G + g;
+                    float* base =
+                        p.dq_acc + ((size_t)slice_q * p.Lq + (size_t)qr.p * p.chunk_q) * D + L;
                     if (!mbar_wait(&bar[C::DQFULL], n & 1, w, 80))
                         return;
                     tc_fence_after();
