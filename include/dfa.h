@@ -278,7 +278,11 @@ dfa_status dfa_ring_fwd(const dfa_attn_desc* desc, const dfa_ring_worker* worker
  *   kv_heads_per_group: a divisor of Hkv, or 0 for the library's choice
  *   (the fewest heads per group that still give the group's backward at
  *   least 2432 key tiles of 128 rows, and at least two groups where B*Hkv
- *   allows).
+ *   allows).  With the library's choice, groups of 4 or more heads, the
+ *   call's first and last groups are each cut into a quarter and three
+ *   quarters (the quarter first at the start, last at the end): the first
+ *   upload and the last download, which no compute overlaps, then move a
+ *   quarter of a group.
  *   ws: dfa_attn_step_host_workspace_size(desc, kv_heads_per_group) bytes,
  *   status word first (dfa_stream_status reads the backward's timeouts).
  * desc->o_fp32 must be 0 (DFA_ERR_UNSUPPORTED otherwise).  When the call

@@ -321,7 +321,6 @@ int64_t bwd_block_rows(int G) { return std::max<int64_t>(8192, 65536 / std::max(
 struct Layout {
     std::vector<dfa_pos_map> qmaps, kmaps;
     int64_t chunk_q, chunk_k;
-    int ring;
 };
 
 dfa_status run_fwd(const dfa_attn_desc& d, const Layout& lay, const void* q, const void* k,
@@ -341,7 +340,6 @@ dfa_status run_fwd(const dfa_attn_desc& d, const Layout& lay, const void* q, con
     p.nkv = (int32_t)lay.kmaps.size();
     p.chunk_q = (int32_t)lay.chunk_q;
     p.chunk_k = (int32_t)lay.chunk_k;
-    p.ring = lay.ring;
     p.causal = d.causal;
     p.scale = d.scale;
     p.scale_log2 = d.scale * 1.4426950408889634f;
@@ -394,7 +392,6 @@ dfa_status run_bwd_main(const dfa_attn_desc& d, const Layout& lay, const void* q
     p.nkv = (int32_t)lay.kmaps.size();
     p.chunk_q = (int32_t)lay.chunk_q;
     p.chunk_k = (int32_t)lay.chunk_k;
-    p.ring = lay.ring;
     p.causal = d.causal;
     p.scale = d.scale;
     p.scale_log2 = d.scale * 1.4426950408889634f;
@@ -455,12 +452,10 @@ Layout whole_layout(const dfa_attn_desc& d)
     if (nc == 1) {
         lay.qmaps.push_back(identity_map(d.N));
         lay.chunk_q = d.N;
-        lay.ring = 0;
     } else {
         for (int p = 0; p < nc; ++p)
             lay.qmaps.push_back(partition_map(d, p));
         lay.chunk_q = d.N / d.P;
-        lay.ring = 1;
     }
     lay.kmaps = lay.qmaps;
     lay.chunk_k = lay.chunk_q;
@@ -606,7 +601,6 @@ dfa_status dfa_chunk_fwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, 
     lay.kmaps.push_back(pair->kv);
     lay.chunk_q = Lq;
     lay.chunk_k = Lk;
-    lay.ring = 0;
     return run_fwd(*desc, lay, q, k, v, o_part, lse_part, 1, ws, (cudaStream_t)stream);
 }
 
@@ -700,7 +694,6 @@ dfa_status dfa_chunk_bwd(const dfa_attn_desc* desc, const dfa_chunk_pair* pair, 
     lay.kmaps.push_back(pair->kv);
     lay.chunk_q = Lq;
     lay.chunk_k = Lk;
-    lay.ring = 0;
     return run_bwd_main(*desc, lay, q, k, v, dout, aug_lse, aug_delta, dq_acc, dk_acc, dv_acc, 1,
                         ws, st);
 }

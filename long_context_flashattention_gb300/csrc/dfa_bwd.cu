@@ -138,10 +138,14 @@ __device__ __forceinline__ QRange clamp_block(const BwdParams& pr, const Unit& u
     return r;
 }
 
+// Step s visits query chunk s: every unit takes the chunks in the same order
+// (not rotated by its own chunk as a ring of workers would), so the units
+// running at one time read the same chunk's Q / dO tiles and add into the
+// same chunk's dQ rows, out of L2.
 __device__ __forceinline__ QRange q_range(const BwdParams& pr, const Unit& un, int s)
 {
     QRange r;
-    r.p = pr.ring ? (un.chunk + s) % pr.nq : s;
+    r.p = s;
     const int32_t nqt = ceil_div(pr.chunk_q, BQ);
     if (!pr.causal && pr.ndocs == 0) {
         r.i0 = 0;

@@ -64,6 +64,9 @@ struct Cfg {
 // documents), an interval of each key chunk because positions increase along
 // a chunk.  Union over the unit's rows: [doc_lo(x_min), upper(x_max)];
 // intersection: [doc_lo(x_max), upper(x_min)].
+// Step s visits key chunk s: every unit takes the chunks in the same order
+// (not rotated by its own chunk as a ring of workers would), so the units
+// running at one time read the same chunk's K/V tiles out of L2.
 struct StepTiles {
     int32_t c, j0, jv, jf0, jf;
 };
@@ -71,7 +74,7 @@ struct StepTiles {
 __device__ __forceinline__ StepTiles step_tiles(const FwdParams& p, const Unit& un, int s)
 {
     StepTiles r;
-    r.c = p.ring ? (un.chunk - s + p.nkv) % p.nkv : s;
+    r.c = s;
     const DevMap& km = p.kmap[r.c];
     if (!p.causal && p.ndocs == 0) {
         r.j0 = 0;

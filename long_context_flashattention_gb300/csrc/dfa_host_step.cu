@@ -18,6 +18,7 @@
 // output slot directly, and in_free[s] is recorded after the backward.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -217,9 +218,41 @@ struct HostStep {
     float* lse;
 };
 
-// nsteps steps as one stream of (step, group) items: item i is group
-// i % groups of step i / groups, so the uploads of a step's first groups
-// overlap the compute of the previous step's last groups.
+// One unit of streamed work: key/value heads [h0, h0 + gk) of batch entry b
+// of step t, with their query heads.
+struct Item {
+    int32_t t, b, h0, gk;
+};
+
+// The (step, group) items of nsteps steps, in order: step-major, groups of
+// pl.gk key/value heads inside a step, so the uploads of a step's first
+// groups overlap the compute of the previous step's last groups.  Only the
+// first upload and the last download of the whole call overlap nothing; with
+// the library's own group size (ramp = true) the first and the last item are
+// cut into a quarter and three quarters, so that those two copies move a
+// quarter of a group.
+std::vector<Item> make_items(const dfa_attn_desc& d, const Plan& pl, int32_t nsteps, bool ramp)
+{
+    std::vector<Item> it;
+    const int per_b = d.Hkv / pl.gk;
+    for (int32_t t = 0; t < nsteps; ++t)
+        for (int g = 0; g < pl.groups; ++g)
+            it.push_back({t, g / per_b, (g % per_b) * pl.gk, pl.gk});
+    if (ramp && pl.gk >= 4) {
+        const int32_t q = pl.gk / 4;
+        Item f = it.front();
+        it.front() = {f.t, f.b, f.h0, q};
+        it.insert(it.begin() + 1, Item{f.t, f.b, f.h0 + q, f.gk - q});
+        Item l = it.back();
+        if (l.gk >= 4) {
+            const int32_t ql = l.gk / 4;
+            it.back() = {l.t, l.b, l.h0, l.gk - ql};
+            it.push_back({l.t, l.b, l.h0 + l.gk - ql, ql});
+        }
+    }
+    return it;
+}
+
 dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* hs,
                      int32_t kv_heads_per_group, void* ws, size_t ws_bytes, void* compute_stream,
                      void* h2d_stream, void* d2h_stream)
@@ -256,55 +289,63 @@ dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* 
         return cuda_err(e, "entry ordering");
 
     char* base = (char*)ws;
-    const int per_b = desc->Hkv / pl.gk;
     const int r = desc->Hq / desc->Hkv;
-    const int64_t heads_q = pl.gd.Hq, heads_k = pl.gk;
     const int64_t d = desc->d;
-    const int64_t items = (int64_t)nsteps * pl.groups;
-    auto host_off_q = [&](int g) {  // element offset of group g in a [B,Hq,N,d] tensor
-        return ((int64_t)(g / per_b) * desc->Hq + (int64_t)(g % per_b) * pl.gk * r) * desc->N;
+    const std::vector<Item> work = make_items(*desc, pl, nsteps, kv_heads_per_group == 0);
+    const int64_t items = (int64_t)work.size();
+    // element offsets of an item's first query / key row in [B,H,N,d] tensors
+    auto host_off_q = [&](const Item& w) {
+        return ((int64_t)w.b * desc->Hq + (int64_t)w.h0 * r) * desc->N;
     };
-    auto host_off_k = [&](int g) {
-        return ((int64_t)(g / per_b) * desc->Hkv + (int64_t)(g % per_b) * pl.gk) * desc->N;
+    auto host_off_k = [&](const Item& w) {
+        return ((int64_t)w.b * desc->Hkv + w.h0) * desc->N;
     };
+    // bytes of an item's q (= o, dq, dO), k (= v, dk, dv) and lse
+    auto q_bytes = [&](const Item& w) { return (size_t)w.gk * r * desc->N * d * 2; };
+    auto k_bytes = [&](const Item& w) { return (size_t)w.gk * desc->N * d * 2; };
+    auto l_bytes = [&](const Item& w) { return (size_t)w.gk * r * desc->N * 4; };
     auto upload = [&](int64_t i) -> cudaError_t {
-        const int s = (int)(i % 2), g = (int)(i % pl.groups);
-        const HostStep& h = hs[i / pl.groups];
+        const int s = (int)(i % 2);
+        const Item& w = work[i];
+        const HostStep& h = hs[w.t];
         const InSet in = in_set(base + pl.off_in[s], pl);
-        const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
+        const int64_t oq = host_off_q(w) * d * 2, ok = host_off_k(w) * d * 2;
+        const size_t qb = q_bytes(w), kb = k_bytes(w);
         cudaError_t x = cudaSuccess;
         if (i >= 2)
             x = cudaStreamWaitEvent(up, ev.e[Events::kInFree0 + s], 0);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.q, (const char*)h.q + oq, pl.qb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.q, (const char*)h.q + oq, qb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.k, (const char*)h.k + ok, pl.kb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.k, (const char*)h.k + ok, kb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.v, (const char*)h.v + ok, pl.kb, cudaMemcpyHostToDevice, up);
+            x = cudaMemcpyAsync(in.v, (const char*)h.v + ok, kb, cudaMemcpyHostToDevice, up);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync(in.dout, (const char*)h.dout + oq, pl.qb, cudaMemcpyHostToDevice,
+            x = cudaMemcpyAsync(in.dout, (const char*)h.dout + oq, qb, cudaMemcpyHostToDevice,
                                 up);
         if (x == cudaSuccess)
             x = cudaEventRecord(ev.e[Events::kUp0 + s], up);
         return x;
     };
     auto download = [&](int64_t i) -> cudaError_t {
-        const int s = (int)(i % 2), g = (int)(i % pl.groups);
-        const HostStep& h = hs[i / pl.groups];
+        const int s = (int)(i % 2);
+        const Item& w = work[i];
+        const HostStep& h = hs[w.t];
         const OutSet out = out_set(base + pl.off_out[s], pl);
-        const int64_t oq = host_off_q(g) * d * 2, ok = host_off_k(g) * d * 2;
-        const int64_t ol = host_off_q(g) * 4;
+        const int64_t oq = host_off_q(w) * d * 2, ok = host_off_k(w) * d * 2;
+        const int64_t ol = host_off_q(w) * 4;
+        const size_t qb = q_bytes(w), kb = k_bytes(w), lb = l_bytes(w);
         cudaError_t x = cudaStreamWaitEvent(dn, ev.e[Events::kDone], 0);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h.o + oq, out.o, pl.qb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.o + oq, out.o, qb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h.lse + ol, out.lse, pl.lb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.lse + ol, out.lse, lb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h.dq + oq, out.dq, pl.qb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dq + oq, out.dq, qb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h.dk + ok, out.dk, pl.kb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dk + ok, out.dk, kb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
-            x = cudaMemcpyAsync((char*)h.dv + ok, out.dv, pl.kb, cudaMemcpyDeviceToHost, dn);
+            x = cudaMemcpyAsync((char*)h.dv + ok, out.dv, kb, cudaMemcpyDeviceToHost, dn);
         if (x == cudaSuccess)
             x = cudaEventRecord(ev.e[Events::kDown0 + s], dn);
         return x;
@@ -315,7 +356,9 @@ dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* 
         const OutSet out = out_set(base + pl.off_out[s], pl);
         const InSet pin = pl.ident ? in : in_set(base + pl.off_pin, pl);
         const OutSet pout = pl.ident ? out : out_set(base + pl.off_pout, pl);
-        const dfa_attn_desc* gd = &pl.gd;
+        const dfa_attn_desc item_desc = group_desc(*desc, work[i].gk);
+        const dfa_attn_desc* gd = &item_desc;
+        const int64_t heads_q = item_desc.Hq, heads_k = item_desc.Hkv;
         cudaError_t x = cudaStreamWaitEvent(cs, ev.e[Events::kUp0 + s], 0);
         if (x != cudaSuccess)
             return cuda_err(x, "stream wait");

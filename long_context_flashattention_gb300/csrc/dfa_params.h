@@ -195,7 +195,6 @@ struct FwdParams {
     int32_t Lq, Lk;              // rows per head slice in q / kv storage
     int32_t nq, nkv;             // chunks per side
     int32_t chunk_q, chunk_k;    // rows per chunk
-    int32_t ring;                // 1: query chunk p meets kv chunks (p - s) mod nkv
     int32_t causal;
     float scale, scale_log2;
     int32_t total_units;
@@ -217,7 +216,6 @@ struct BwdParams {
     int32_t Lq, Lk;
     int32_t nq, nkv;
     int32_t chunk_q, chunk_k;
-    int32_t ring;                // 1: kv chunk c meets query chunks (c + s) mod nq
     int32_t causal;
     float scale, scale_log2;
     int32_t total_units;

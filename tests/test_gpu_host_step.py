@@ -123,3 +123,35 @@ def test_steps_host_equals_single_steps():
         assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
         for a, b in zip(got[2:], ref[2:]):
             assert float((a.float() - b.float()).norm() / b.float().norm()) <= 2e-3
+
+
+@pytest.mark.parametrize("kind,P,Hq,Hkv", [("striped", 2, 8, 8), ("balanced", 2, 16, 8)])
+def test_steps_host_library_groups_cut_first_and_last(orc, kind, P, Hq, Hkv):
+    """The library's own grouping (kv_heads_per_group = 0) at 8 key/value
+    heads: two groups of 4 per step, and the call's first and last groups cut
+    into 1 + 3 and 3 + 1 heads.  Two steps in one call give, per step, what
+    explicit groups of 4 give (O and LSE bit for bit, gradients to fp32
+    atomic-order noise), and the oracle's result on a sampled head of every
+    cut group."""
+    B, N, d = 1, 1024, 128
+    steps = [_pinned(*make_qkvdo(B, Hq, Hkv, N, d, seed=300 + t)) for t in range(2)]
+    multi = dfa.attn_steps_host(steps, P=P, partition=kind, kv_heads_per_group=0)
+    torch.cuda.synchronize()
+    r = Hq // Hkv
+    for t, (st, got) in enumerate(zip(steps, multi)):
+        ref = _step_host(*st, P=P, partition=kind, kv_heads_per_group=4)
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+        for a, b in zip(got[2:], ref[2:]):
+            assert float((a.float() - b.float()).norm() / b.float().norm()) <= 2e-3
+        # head 0 (first cut of step 0) and head 7 (last cut of step 1) against the oracle
+        hk = 0 if t == 0 else Hkv - 1
+        qs = slice(hk * r, hk * r + r)
+        q, do = (x[:, qs].contiguous() for x in (st[0], st[3]))
+        k, v = (x[:, hk:hk + 1].contiguous() for x in (st[1], st[2]))
+        O, L = orc.attn_fwd(q, k, v)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do)
+        check_o(got[0][:, qs], O)
+        check_lse(got[1][:, qs], L)
+        check_grad(got[2][:, qs], dq, "dQ")
+        check_grad(got[3][:, hk:hk + 1], dk, "dK")
+        check_grad(got[4][:, hk:hk + 1], dv, "dV")
