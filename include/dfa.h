@@ -266,10 +266,15 @@ dfa_status dfa_ring_fwd(const dfa_attn_desc* desc, const dfa_ring_worker* worker
  * group is a complete problem of B = 1).  Group g's upload (h2d_stream), its
  * compute (compute_stream) and its download (d2h_stream) are ordered by
  * events, so that group g+1 uploads and group g-1 downloads while group g
- * computes; device staging is double-buffered in ws.  With pinned host
- * memory the copies overlap the compute; pageable memory gives the same
- * results with the copies serialised by the driver.  h2d_stream or
- * d2h_stream NULL: those copies run on compute_stream, in order.
+ * computes; device staging is double-buffered in ws.  When either copy
+ * stream is given, odd groups compute on a stream the call creates (and
+ * releases) and even groups on compute_stream, so that a group's forward
+ * starts on the SMs the previous group's backward releases; the backwards
+ * themselves run one after another.  With pinned host memory the copies
+ * overlap the compute; pageable memory gives the same results with the
+ * copies serialised by the driver.  h2d_stream or d2h_stream NULL: those
+ * copies run on compute_stream, in order (and with both NULL, everything
+ * runs on compute_stream).
  *   h_q, h_dout [B,Hq,N,d] bf16; h_k, h_v [B,Hkv,N,d] bf16 (read);
  *   h_o, h_dq [B,Hq,N,d] bf16, h_lse [B,Hq,N] fp32, h_dk, h_dv [B,Hkv,N,d]
  *   bf16 (written; O is the forward output, LSE its natural-log row

@@ -6,10 +6,12 @@
 // Host code only.  Per group g (slot s = g % 2 of the double-buffered
 // staging):
 //   h2d stream:      [wait in_free[s]]  upload q, k, v, dO of g  -> up[s]
-//   compute stream:  wait up[s]; permute in -> in_free[s]; [wait down[s]]
-//                    forward; backward; permute out into out staging[s]
-//                    -> done
+//   compute stream s: wait up[s]; permute in -> in_free[s]; [wait down[s]]
+//                    forward; [wait bwd]; backward -> bwd; permute out into
+//                    out staging[s] -> done
 //   d2h stream:      wait done; download o, lse, dq, dk, dv of g -> down[s]
+// (compute stream 0 is the caller's, stream 1 the call's own when the copies
+// have streams of their own; otherwise both are the caller's).
 // in_free[s] lets the upload of g+2 reuse the input slot once g's inputs are
 // consumed; down[s] keeps the compute of g+2 from overwriting the output
 // slot before g's download has read it.  When the partition's storage order
@@ -97,7 +99,8 @@ struct Plan {
     size_t qb = 0, kb = 0, lb = 0;      // one group's q (= o, dq, dO), k (= v, dk, dv), lse
     size_t bwd_ws = 0;                   // the group backward's workspace (status word first)
     size_t in_set = 0, out_set = 0;      // one input set (q k v dO), one output set
-    size_t off_in[2] = {0, 0}, off_out[2] = {0, 0}, off_pin = 0, off_pout = 0, total = 0;
+    size_t off_in[2] = {0, 0}, off_out[2] = {0, 0}, off_pin[2] = {0, 0}, off_pout[2] = {0, 0};
+    size_t total = 0;
 };
 
 dfa_status make_plan(const dfa_attn_desc* desc, int32_t kv_heads_per_group, Plan& pl)
@@ -133,12 +136,14 @@ dfa_status make_plan(const dfa_attn_desc* desc, int32_t kv_heads_per_group, Plan
         pl.off_out[s] = off;
         off += pl.out_set;
     }
-    pl.off_pin = pl.off_pout = off;
-    if (!pl.ident) {  // the worker-major copies the kernels read and write
-        pl.off_pin = off;
-        off += pl.in_set;
-        pl.off_pout = off;
-        off += pl.out_set;
+    for (int s = 0; s < 2; ++s) {
+        pl.off_pin[s] = pl.off_pout[s] = off;
+        if (!pl.ident) {  // the worker-major copies the kernels read and write
+            pl.off_pin[s] = off;
+            off += pl.in_set;
+            pl.off_pout[s] = off;
+            off += pl.out_set;
+        }
     }
     pl.total = off;
     return DFA_OK;
@@ -175,7 +180,10 @@ OutSet out_set(char* base, const Plan& pl)
 }
 
 struct Events {
-    enum { kEntry, kUp0, kUp1, kInFree0, kInFree1, kDone, kDown0, kDown1, kTailUp, kCount };
+    enum {
+        kEntry, kUp0, kUp1, kInFree0, kInFree1, kDone, kDown0, kDown1, kTailUp, kBwd, kTail1,
+        kCount
+    };
     cudaEvent_t e[kCount] = {};
     ~Events()
     {
@@ -288,6 +296,30 @@ dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* 
     if (e != cudaSuccess)
         return cuda_err(e, "entry ordering");
 
+    // Two compute streams when the copies run beside the compute: items of
+    // slot 0 on compute_stream, items of slot 1 on a stream of the call's
+    // own, so that one group's forward starts on the SMs that the previous
+    // group's backward releases in its last wave.  Each slot has its own
+    // staging and worker-major copies; the backwards share the workspace's
+    // scratch and run one after another.
+    struct OwnStream {
+        cudaStream_t s = nullptr;
+        ~OwnStream()
+        {
+            if (s)
+                cudaStreamDestroy(s);
+        }
+    } own;
+    cudaStream_t comp[2] = {cs, cs};
+    if (up != cs || dn != cs) {
+        e = cudaStreamCreateWithFlags(&own.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(own.s, ev.e[Events::kEntry], 0);
+        if (e != cudaSuccess)
+            return cuda_err(e, "second compute stream");
+        comp[1] = own.s;
+    }
+
     char* base = (char*)ws;
     const int r = desc->Hq / desc->Hkv;
     const int64_t d = desc->d;
@@ -352,60 +384,68 @@ dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* 
     };
     auto compute = [&](int64_t i) -> dfa_status {
         const int s = (int)(i % 2);
+        const cudaStream_t c = comp[s];
         const InSet in = in_set(base + pl.off_in[s], pl);
         const OutSet out = out_set(base + pl.off_out[s], pl);
-        const InSet pin = pl.ident ? in : in_set(base + pl.off_pin, pl);
-        const OutSet pout = pl.ident ? out : out_set(base + pl.off_pout, pl);
+        const InSet pin = pl.ident ? in : in_set(base + pl.off_pin[s], pl);
+        const OutSet pout = pl.ident ? out : out_set(base + pl.off_pout[s], pl);
         const dfa_attn_desc item_desc = group_desc(*desc, work[i].gk);
         const dfa_attn_desc* gd = &item_desc;
         const int64_t heads_q = item_desc.Hq, heads_k = item_desc.Hkv;
-        cudaError_t x = cudaStreamWaitEvent(cs, ev.e[Events::kUp0 + s], 0);
+        cudaError_t x = cudaStreamWaitEvent(c, ev.e[Events::kUp0 + s], 0);
         if (x != cudaSuccess)
             return cuda_err(x, "stream wait");
         dfa_status t = DFA_OK;
         if (!pl.ident) {
-            t = dfa_permute(gd, 0, in.q, pin.q, 2, d, heads_q, cs);
+            t = dfa_permute(gd, 0, in.q, pin.q, 2, d, heads_q, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 0, in.k, pin.k, 2, d, heads_k, cs);
+                t = dfa_permute(gd, 0, in.k, pin.k, 2, d, heads_k, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 0, in.v, pin.v, 2, d, heads_k, cs);
+                t = dfa_permute(gd, 0, in.v, pin.v, 2, d, heads_k, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 0, in.dout, pin.dout, 2, d, heads_q, cs);
+                t = dfa_permute(gd, 0, in.dout, pin.dout, 2, d, heads_q, c);
             if (t != DFA_OK)
                 return t;
-            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
+            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], c)) != cudaSuccess)
                 return cuda_err(x, "event record");
         }
         // the output slot was last read by the download of item i - 2
-        if (pl.ident && i >= 2 && dn != cs &&
-            (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
+        if (pl.ident && i >= 2 && dn != c &&
+            (x = cudaStreamWaitEvent(c, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
             return cuda_err(x, "stream wait");
-        t = dfa_attn_fwd(gd, pin.q, pin.k, pin.v, pout.o, (float*)pout.lse, ws, 256, cs);
-        if (t == DFA_OK)
-            t = dfa_attn_bwd(gd, pin.q, pin.k, pin.v, pout.o, pin.dout, (const float*)pout.lse,
-                             pout.dq, pout.dk, pout.dv, ws, pl.bwd_ws, cs);
+        t = dfa_attn_fwd(gd, pin.q, pin.k, pin.v, pout.o, (float*)pout.lse, ws, 256, c);
         if (t != DFA_OK)
             return t;
+        // the backwards share one workspace: item i's after item i - 1's
+        if (i >= 1 && comp[1] != comp[0] &&
+            (x = cudaStreamWaitEvent(c, ev.e[Events::kBwd], 0)) != cudaSuccess)
+            return cuda_err(x, "stream wait");
+        t = dfa_attn_bwd(gd, pin.q, pin.k, pin.v, pout.o, pin.dout, (const float*)pout.lse,
+                         pout.dq, pout.dk, pout.dv, ws, pl.bwd_ws, c);
+        if (t != DFA_OK)
+            return t;
+        if ((x = cudaEventRecord(ev.e[Events::kBwd], c)) != cudaSuccess)
+            return cuda_err(x, "event record");
         if (pl.ident) {
-            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], cs)) != cudaSuccess)
+            if ((x = cudaEventRecord(ev.e[Events::kInFree0 + s], c)) != cudaSuccess)
                 return cuda_err(x, "event record");
         } else {
-            if (i >= 2 && dn != cs &&
-                (x = cudaStreamWaitEvent(cs, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
+            if (i >= 2 && dn != c &&
+                (x = cudaStreamWaitEvent(c, ev.e[Events::kDown0 + s], 0)) != cudaSuccess)
                 return cuda_err(x, "stream wait");
-            t = dfa_permute(gd, 1, pout.o, out.o, 2, d, heads_q, cs);
+            t = dfa_permute(gd, 1, pout.o, out.o, 2, d, heads_q, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 1, pout.lse, out.lse, 4, 1, heads_q, cs);
+                t = dfa_permute(gd, 1, pout.lse, out.lse, 4, 1, heads_q, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 1, pout.dq, out.dq, 2, d, heads_q, cs);
+                t = dfa_permute(gd, 1, pout.dq, out.dq, 2, d, heads_q, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 1, pout.dk, out.dk, 2, d, heads_k, cs);
+                t = dfa_permute(gd, 1, pout.dk, out.dk, 2, d, heads_k, c);
             if (t == DFA_OK)
-                t = dfa_permute(gd, 1, pout.dv, out.dv, 2, d, heads_k, cs);
+                t = dfa_permute(gd, 1, pout.dv, out.dv, 2, d, heads_k, c);
             if (t != DFA_OK)
                 return t;
         }
-        if ((x = cudaEventRecord(ev.e[Events::kDone], cs)) != cudaSuccess)
+        if ((x = cudaEventRecord(ev.e[Events::kDone], c)) != cudaSuccess)
             return cuda_err(x, "event record");
         return DFA_OK;
     };
@@ -425,10 +465,16 @@ dfa_status run_steps(const dfa_attn_desc* desc, int32_t nsteps, const HostStep* 
         if ((e = download(i)) != cudaSuccess)
             st = cuda_err(e, "download");
     }
-    // Join: everything queued on the copy streams is ordered before later
-    // work on compute_stream, on success and on error alike.
+    // Join: everything queued on the copy streams and the second compute
+    // stream is ordered before later work on compute_stream, on success and
+    // on error alike.
     cudaError_t j = cudaSuccess;
-    if (up != cs) {
+    if (comp[1] != cs) {
+        j = cudaEventRecord(ev.e[Events::kTail1], comp[1]);
+        if (j == cudaSuccess)
+            j = cudaStreamWaitEvent(cs, ev.e[Events::kTail1], 0);
+    }
+    if (j == cudaSuccess && up != cs) {
         j = cudaEventRecord(ev.e[Events::kTailUp], up);
         if (j == cudaSuccess)
             j = cudaStreamWaitEvent(cs, ev.e[Events::kTailUp], 0);

@@ -230,8 +230,8 @@ def _step_host_ws(desc, gk):
 
 def test_step_host_workspace_layout():
     """Group backward workspace, two input and two output staging slots, and
-    (when the partition's storage order is not natural order) one worker-major
-    input and output set."""
+    (when the partition's storage order is not natural order) a worker-major
+    input and output set per slot (the two slots compute on two streams)."""
     def a256(x):
         return (x + 255) // 256 * 256
 
@@ -244,7 +244,7 @@ def test_step_host_workspace_layout():
         qb, kb, lb = gk * N * d * 2, gk * N * d * 2, gk * N * 4
         in_set, out_set = 2 * a256(qb) + 2 * a256(kb), 2 * a256(qb) + a256(lb) + 2 * a256(kb)
         need = (a256(dfa.workspace_size(gdesc, dfa.OP_BWD)) + 2 * in_set + 2 * out_set +
-                extra * (in_set + out_set))
+                extra * 2 * (in_set + out_set))
         assert _step_host_ws(desc, gk) == need
         assert _step_host_ws(desc, 0) == need     # the automatic choice
     # a token stripe as long as a chunk keeps natural order
