@@ -443,8 +443,10 @@ def run_gpu(args):
             "bound": "tensor", "achieved": round(bwd_tflops, 2), "peak": peak_s,
             "unit": "TFLOP/s", "frac": round(bwd_tflops / peak_s, 4),
             "peak_source": f"{src} bf16_tflops_sustained",
-            "traffic": kernel_traffic("attn_bwd_kernel_llama7b_128k_traffic.md",
-                                      "attn_bwd_kernel"),
+            # the committed DRAM capture covers the 128K workload only
+            "traffic": (kernel_traffic("attn_bwd_kernel_llama7b_128k_traffic.md",
+                                       "attn_bwd_kernel")
+                        if args.workload == "llama7b_128k" and not args.heads else None),
         },
         "merge": {"kernel": "dfa::lse_merge_kernel", "k": P, "rows": rows,
                   "bytes": merge_bytes, "ms": round(merge_ms, 4),
