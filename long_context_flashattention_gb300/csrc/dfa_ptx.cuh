@@ -493,6 +493,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
                  : "memory");
 }
 
+// L2 policy that keeps the lines it touches resident ahead of normal lines.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// *addr += v in L2 (no return value), with an L2 eviction policy.
+__device__ __forceinline__ void red_add_f32(float* addr, float v, uint64_t pol)
+{
+    asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(pol)
+                 : "memory");
+}
+
 // 128-byte swizzle: byte offset of 16-byte chunk `c` (0..7) of row `r` inside
 // a 1024-byte aligned tile whose rows are 128 bytes.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c)
