@@ -360,9 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sv[i] = __uint_as_float(r[i]);
                         if (j < st.jf0 || j >= st.jf || !valid) {
                             const int nv = cnt - j * 128, n0 = lo - j * 128;
+                            if (n0 <= 0) {
+                                // no lower bound inside the tile (always so
+                                // without documents): one compare per key
 #pragma unroll
-                            for (int i = 0; i < 128; ++i)
-                                sv[i] = (i >= n0 && i < nv) ? sv[i] : -INFINITY;
+                                for (int i = 0; i < 128; ++i)
+                                    sv[i] = i < nv ? sv[i] : -INFINITY;
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 128; ++i)
+                                    sv[i] = (i >= n0 && i < nv) ? sv[i] : -INFINITY;
+                            }
                         }
                         // row max, two new values per 3-input max
                         float mx = fmaxf(sv[0], sv[1]);
