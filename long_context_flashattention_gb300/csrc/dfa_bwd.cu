@@ -33,17 +33,19 @@
 //               values (hi + mid + lo, exact to fp32 precision), so the
 //               softmax warps read no per-row data.  S^T and dP^T signal
 //               completion separately.
-//   warp 12     issues dV += P^T dO (on P^T ready), dK += dS^T Q (on dS^T
-//               ready; A operands read from TMEM), then dQ^T = K^T dS^T into
-//               the dP^T columns.  S^T of the next step is issued by warp 14
-//               as soon as dV completes, so it fills the tensor pipe while the
-//               softmax warps form dS^T.
+//   warp 12     issues dV += P^T dO (on P^T ready), then, on dS^T ready,
+//               dQ^T = K^T dS^T into the dP^T columns and dK += dS^T Q, both
+//               reading dS^T from its shared-memory tile.  dQ^T goes first:
+//               the next dP^T waits for its columns, which the drain frees
+//               while dK still runs (dK first cost 4 % at 128K).  S^T of the
+//               next step is issued by warp 14 as soon as dV completes, so it
+//               fills the tensor pipe while the softmax warps form dS^T.
 //   warps 0-7   two warpgroups, one thread per key row, warpgroup h on query
 //               columns [64 h, 64 h + 64) of each step, in two halves of 32:
 //               P^T = exp2(S^T c), packed (bf16) into its own columns of the
-//               S^T region and signalled; then dS^T = P^T (dP^T - D) packed
-//               into the dP^T region and stored into the swizzled SMEM tile
-//               that is the B operand of dQ^T.  At the end of a unit the
+//               S^T region and signalled; then dS^T = P^T (dP^T - D) stored
+//               into the swizzled SMEM tile that is the B operand of dQ^T
+//               and the A operand of dK.  At the end of a unit the
 //               first warpgroup stores dK (scaled), the second dV.
 //   warps 8-11  drain each step's dQ^T tile from TMEM (all 128 columns into
 //               registers, which frees the columns for the next dP^T) and add
@@ -101,14 +103,15 @@ struct Cfg {
     // records; emptied by two arrivals: dP^T and dV have read it).
     // SFULL: S^T of a step computed; DPFULL: its dP^T computed; PREADY: its
     // P^T written to TMEM; PVDONE: its dV computed (P^T consumed, the S^T
-    // columns free); DSREADY: its dS^T written (TMEM and SMEM); DQFULL: its
-    // dQ^T computed (hence its dK too, issued before it by the same thread);
-    // DQEMPTY: dQ^T read out of TMEM (the dP^T columns free).
+    // columns free); DSREADY: its dS^T tile written; DQFULL: its dQ^T
+    // computed; DQEMPTY: dQ^T read out of TMEM (the dP^T columns free);
+    // DKDONE: its dK computed (the dS^T tile and the Q stage read: dK is the
+    // step's last MMA); DKVFULL: all of the unit's MMAs complete.
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
                          DOFULL = QEMPTY + kQStages, DOEMPTY = DOFULL + 1, SFULL = DOEMPTY + 1,
                          DPFULL = SFULL + 1, PREADY = DPFULL + 1, PVDONE = PREADY + 1,
                          DSREADY = PVDONE + 1, DQFULL = DSREADY + 1, DQEMPTY = DQFULL + 1,
-                         DKVFULL = DQEMPTY + 1, NBAR = DKVFULL + 1;
+                         DKVFULL = DQEMPTY + 1, DKDONE = DKVFULL + 1, NBAR = DKDONE + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t cDK = 0, cDV = D, cS = 2 * D, cDP = 2 * D + 128;
 };
@@ -194,7 +197,7 @@ __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& u
     return t * pr.G;
 }
 
-// TMEM column of the packed bf16 P^T / dS^T for K step kk (16 query rows):
+// TMEM column of the packed bf16 P^T for K step kk (16 query rows):
 // warpgroup h's query columns [64 h, 64 h + 64) are packed at columns
 // [64 h, 64 h + 32) of the region (its own columns, so that neither
 // warpgroup overwrites values the other has still to read).
@@ -312,8 +315,10 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 // Warp 12 (issue_grads), per step n:
 //   dV += P^T(n) dO(n)    once the softmax warps have written P^T (and dO(n)
 //                         has landed);
-//   dK += dS^T(n) Q(n)    once they have written dS^T (A operands from TMEM);
-//   dQ^T(n) = K^T dS^T(n) into the dP^T columns.
+//   dQ^T(n) = K^T dS^T(n) into the dP^T columns, once they have written the
+//                         dS^T tile;
+//   dK += dS^T(n) Q(n)    from the same tile, after dQ^T so that the drain
+//                         reads dQ^T (and frees the dP^T columns) meanwhile.
 template <int D>
 __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared& sh,
                                                const WaitCtx& w)
@@ -382,6 +387,7 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
     const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO), BQ * 128, 1024);
     const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
     const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs), 16384, 1024);
+    const uint64_t dDsk = sdesc_sw128(smem_u32(sh.smem + C::kDs), 16, 1024);
     uint32_t uc = 0, n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = bwd_unit(p, u);
@@ -408,22 +414,23 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
                        (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&bar[C::PVDONE]);
             tc_commit(&bar[C::DOEMPTY]);  // second arrival: dV has read dO
-            // dK += dS^T Q
             if (!mbar_wait(&bar[C::DSREADY], ph, w, 67))
                 return;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ts(tmem + C::cDK, tmem + C::cDP + ptcol(kk),
-                       sdesc_add(dQm, qs * C::kQTile + kk * 2048), idKV,
-                       (it > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bar[C::QEMPTY + qs]);
             // dQ^T [128 x BQ] = K^T [128 x kv] dS^T [kv x BQ], into the dP^T columns
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 mma_ss(tmem + C::cDP, sdesc_add(dKm, kk * 2048), sdesc_add(dDsm, kk * 2048), idQ,
                        kk > 0);
             tc_commit(&bar[C::DQFULL]);
+            // dK += dS^T Q, dS^T from the shared-memory tile
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)
+                mma_ss(tmem + C::cDK, sdesc_add(dDsk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                       sdesc_add(dQm, qs * C::kQTile + kk * 2048), idKV,
+                       (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&bar[C::QEMPTY + qs]);
+            tc_commit(&bar[C::DKDONE]);
         }
         // all of the unit's MMAs are complete once these land: the S^T / dP^T
         // of its last step completed before its softmax, hence before its dK
@@ -531,8 +538,8 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         if (!mbar_wait(&bar[C::DPFULL], ph, w, 70))
                             return;
                         tc_fence_after();
-                        // the dQ^T of step n - 1 has read the dS^T tile
-                        if (n >= 1 && !mbar_wait(&bar[C::DQFULL], (n - 1) & 1, w, 72))
+                        // the dK of step n - 1 has read the dS^T tile
+                        if (n >= 1 && !mbar_wait(&bar[C::DKDONE], (n - 1) & 1, w, 72))
                             return;
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
@@ -550,13 +557,11 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                          d0, d1);
                                 dd[j] = pack_bf16x2(d0, d1);
                             }
-                            tmem_st16(tDP + 16 * c, dd);
 #pragma unroll
                             for (int ch = 0; ch < 4; ++ch)
                                 st_shared_v4(dsb_s + sw128_offset(r, 4 * c + ch), dd[4 * ch],
                                              dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
                         }
-                        tmem_st_wait();
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(&bar[C::DSREADY]);
@@ -746,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar[C::DQFULL], 1);
         mbar_init(&bar[C::DQEMPTY], 128);
         mbar_init(&bar[C::DKVFULL], 1);
+        mbar_init(&bar[C::DKDONE], 1);
         fence_barrier_init();
     }
     {
