@@ -24,8 +24,9 @@
 //               its rows' -LSE/scale records into a 2-stage ring, and the dO
 //               tile with its rows' -D records into a single stage that is
 //               refilled as soon as dP^T and dV of the step have read it.
-//   warp 14     issues S^T = K Q^T - LSE/scale (once dV of the previous step
-//               has consumed P^T, whose columns S^T overwrites) and
+//   warp 14     issues S^T = K Q^T - LSE/scale (once dK of the previous step
+//               has read the dS^T packed into the S^T columns; dV, issued
+//               before dK, has read P^T there) and
 //               dP^T = V dO^T - D (once the previous dQ^T has been drained
 //               from the columns dP^T overwrites).  The row constants enter
 //               as one more K = 16 slice of each product: a ones tile against
@@ -34,18 +35,19 @@
 //               softmax warps read no per-row data.  S^T and dP^T signal
 //               completion separately.
 //   warp 12     issues dV += P^T dO (on P^T ready), then, on dS^T ready,
-//               dQ^T = K^T dS^T into the dP^T columns and dK += dS^T Q, both
-//               reading dS^T from its shared-memory tile.  dQ^T goes first:
-//               the next dP^T waits for its columns, which the drain frees
-//               while dK still runs (dK first cost 4 % at 128K).  S^T of the
-//               next step is issued by warp 14 as soon as dV completes, so it
-//               fills the tensor pipe while the softmax warps form dS^T.
+//               dQ^T = K^T dS^T into the dP^T columns (B operand: the dS^T
+//               tile in shared memory) and dK += dS^T Q (A operand: dS^T
+//               packed in TMEM, in the half of the S^T columns that P^T
+//               leaves free).  dQ^T goes first: the next dP^T waits for its
+//               columns, which the drain frees while dK still runs (dK first
+//               cost 4 % at 128K).
 //   warps 0-7   two warpgroups, one thread per key row, warpgroup h on query
 //               columns [64 h, 64 h + 64) of each step, in two halves of 32:
 //               P^T = exp2(S^T c), packed (bf16) into its own columns of the
-//               S^T region and signalled; then dS^T = P^T (dP^T - D) stored
-//               into the swizzled SMEM tile that is the B operand of dQ^T
-//               and the A operand of dK.  At the end of a unit the
+//               S^T region and signalled; then dS^T = P^T (dP^T - D) packed
+//               into the other half of those columns (dK's A operand) and
+//               stored into the swizzled SMEM tile that is the B operand of
+//               dQ^T.  At the end of a unit the
 //               first warpgroup stores dK (scaled), the second dV.
 //   warps 8-11  drain each step's dQ^T tile from TMEM (all 128 columns into
 //               registers, which frees the columns for the next dP^T) and add
@@ -102,15 +104,15 @@ struct Cfg {
     // -LSE/scale records); DOFULL/DOEMPTY: the dO stage (with its -D
     // records; emptied by two arrivals: dP^T and dV have read it).
     // SFULL: S^T of a step computed; DPFULL: its dP^T computed; PREADY: its
-    // P^T written to TMEM; PVDONE: its dV computed (P^T consumed, the S^T
-    // columns free); DSREADY: its dS^T tile written; DQFULL: its dQ^T
-    // computed; DQEMPTY: dQ^T read out of TMEM (the dP^T columns free);
-    // DKDONE: its dK computed (the dS^T tile and the Q stage read: dK is the
-    // step's last MMA); DKVFULL: all of the unit's MMAs complete.
+    // P^T written to TMEM; DSREADY: its dS^T written (TMEM and the SMEM
+    // tile); DQFULL: its dQ^T computed; DQEMPTY: dQ^T read out of TMEM (the
+    // dP^T columns free); DKDONE: its dK computed (dK is the step's last MMA:
+    // the S^T columns, the dS^T tile and the Q stage are all read);
+    // DKVFULL: all of the unit's MMAs complete.
     static constexpr int KVFULL = 0, KVEMPTY = 1, QFULL = 2, QEMPTY = QFULL + kQStages,
                          DOFULL = QEMPTY + kQStages, DOEMPTY = DOFULL + 1, SFULL = DOEMPTY + 1,
-                         DPFULL = SFULL + 1, PREADY = DPFULL + 1, PVDONE = PREADY + 1,
-                         DSREADY = PVDONE + 1, DQFULL = DSREADY + 1, DQEMPTY = DQFULL + 1,
+                         DPFULL = SFULL + 1, PREADY = DPFULL + 1, DSREADY = PREADY + 1,
+                         DQFULL = DSREADY + 1, DQEMPTY = DQFULL + 1,
                          DKVFULL = DQEMPTY + 1, DKDONE = DKVFULL + 1, NBAR = DKDONE + 1;
     static constexpr int kSmem = kBar + NBAR * 8 + 16 + 1024;
     static constexpr uint32_t cDK = 0, cDV = D, cS = 2 * D, cDP = 2 * D + 128;
@@ -197,7 +199,8 @@ __device__ __forceinline__ int32_t unit_steps(const BwdParams& pr, const Unit& u
     return t * pr.G;
 }
 
-// TMEM column of the packed bf16 P^T for K step kk (16 query rows):
+// TMEM column of the packed bf16 P^T for K step kk (16 query rows; the
+// packed dS^T sits 32 columns further):
 // warpgroup h's query columns [64 h, 64 h + 64) are packed at columns
 // [64 h, 64 h + 32) of the region (its own columns, so that neither
 // warpgroup overwrites values the other has still to read).
@@ -308,17 +311,19 @@ __device__ __forceinline__ void producer(const BwdParams& p, const Shared& sh, c
 // completion barrier, never through issue order.
 //
 // Warp 14 (issue_products), per step m:
-//   S^T(m) = K Q(m)^T - LSE/scale   once Q(m) has landed and dV(m-1) has
-//                                   consumed P^T(m-1) (same columns);
+//   S^T(m) = K Q(m)^T - LSE/scale   once Q(m) has landed and dK(m-1) has
+//                                   read dS^T(m-1) from the same columns
+//                                   (dV(m-1), issued before it, P^T(m-1));
 //   dP^T(m) = V dO(m)^T - D         once dO(m) has landed and dQ^T(m-1) has
 //                                   been read out of the same columns.
 // Warp 12 (issue_grads), per step n:
 //   dV += P^T(n) dO(n)    once the softmax warps have written P^T (and dO(n)
 //                         has landed);
-//   dQ^T(n) = K^T dS^T(n) into the dP^T columns, once they have written the
-//                         dS^T tile;
-//   dK += dS^T(n) Q(n)    from the same tile, after dQ^T so that the drain
-//                         reads dQ^T (and frees the dP^T columns) meanwhile.
+//   dQ^T(n) = K^T dS^T(n) into the dP^T columns, once they have written
+//                         dS^T (B operand: the SMEM tile);
+//   dK += dS^T(n) Q(n)    A operand: dS^T packed in the S^T columns; after
+//                         dQ^T so that the drain reads dQ^T (and frees the
+//                         dP^T columns) meanwhile.
 template <int D>
 __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared& sh,
                                                const WaitCtx& w)
@@ -347,7 +352,7 @@ __device__ __forceinline__ void issue_products(const BwdParams& p, const Shared&
             const uint32_t qs = m % C::kQStages;
             if (!mbar_wait(&bar[C::QFULL + qs], (m / C::kQStages) & 1, w, 61))
                 return;
-            if (m >= 1 && !mbar_wait(&bar[C::PVDONE], (m - 1) & 1, w, 62))
+            if (m >= 1 && !mbar_wait(&bar[C::DKDONE], (m - 1) & 1, w, 62))
                 return;
             tc_fence_after();
 #pragma unroll
@@ -387,7 +392,6 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
     const uint64_t dDOm = sdesc_sw128(smem_u32(sh.smem + C::kDO), BQ * 128, 1024);
     const uint64_t dKm = sdesc_sw128(smem_u32(sh.smem + C::kK), 16384, 1024);
     const uint64_t dDsm = sdesc_sw128(smem_u32(sh.smem + C::kDs), 16384, 1024);
-    const uint64_t dDsk = sdesc_sw128(smem_u32(sh.smem + C::kDs), 16, 1024);
     uint32_t uc = 0, n = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
         Unit un = bwd_unit(p, u);
@@ -412,7 +416,6 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
             for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ts(tmem + C::cDV, tmem + C::cS + ptcol(kk), sdesc_add(dDOm, kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bar[C::PVDONE]);
             tc_commit(&bar[C::DOEMPTY]);  // second arrival: dV has read dO
             if (!mbar_wait(&bar[C::DSREADY], ph, w, 67))
                 return;
@@ -426,7 +429,7 @@ __device__ __forceinline__ void issue_grads(const BwdParams& p, const Shared& sh
             // dK += dS^T Q, dS^T from the shared-memory tile
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ss(tmem + C::cDK, sdesc_add(dDsk, (kk >> 2) * 16384 + (kk & 3) * 32),
+                mma_ts(tmem + C::cDK, tmem + C::cS + 32 + ptcol(kk),
                        sdesc_add(dQm, qs * C::kQTile + kk * 2048), idKV,
                        (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&bar[C::QEMPTY + qs]);
@@ -538,7 +541,9 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                         if (!mbar_wait(&bar[C::DPFULL], ph, w, 70))
                             return;
                         tc_fence_after();
-                        // the dK of step n - 1 has read the dS^T tile
+                        // dQ^T and dK of step n - 1 have read the dS^T tile
+                        // and the packed dS^T (implied by S^T(n), which
+                        // was issued after dK(n - 1))
                         if (n >= 1 && !mbar_wait(&bar[C::DKDONE], (n - 1) & 1, w, 72))
                             return;
 #pragma unroll
@@ -557,11 +562,13 @@ __device__ __forceinline__ void softmax_grad(const BwdParams& p, const Shared& s
                                          d0, d1);
                                 dd[j] = pack_bf16x2(d0, d1);
                             }
+                            tmem_st16(tS + 32 + 16 * c, dd);
 #pragma unroll
                             for (int ch = 0; ch < 4; ++ch)
                                 st_shared_v4(dsb_s + sw128_offset(r, 4 * c + ch), dd[4 * ch],
                                              dd[4 * ch + 1], dd[4 * ch + 2], dd[4 * ch + 3]);
                         }
+                        tmem_st_wait();
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(&bar[C::DSREADY]);
@@ -746,7 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar[C::SFULL], 1);
         mbar_init(&bar[C::DPFULL], 1);
         mbar_init(&bar[C::PREADY], 256);
-        mbar_init(&bar[C::PVDONE], 1);
         mbar_init(&bar[C::DSREADY], 256);
         mbar_init(&bar[C::DQFULL], 1);
         mbar_init(&bar[C::DQEMPTY], 128);
