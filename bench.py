@@ -147,6 +147,19 @@ def kernel_traffic(summary: str, kernel: str):
         return None
 
 
+def schedule_summary(N: int, P: int, kind: str) -> dict:
+    """How evenly the workload's partition spreads the causal (query, key)
+    pairs over a P-worker ring (dfa_make_schedule, host only; Striped
+    Attention Guide, "Workload Balance Theorem"; DistFlashAttn Guide, "The
+    Causal Imbalance Crisis"): eta_slots is the share of (worker, step) slots
+    with any work, eta_flops the lockstep utilisation, total pairs over P
+    times the sum of each step's largest per-worker load."""
+    from long_context_flashattention_gb300 import dfa
+    s = dfa.make_schedule(N, P, kind, items=False)
+    return {"P": P, "partition": kind, "total_pairs": s["total_pairs"],
+            "eta_slots": round(s["eta_slots"], 6), "eta_flops": round(s["eta_flops"], 6)}
+
+
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
@@ -469,6 +482,7 @@ def run_gpu(args):
                          "achieved": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
+        "schedule": schedule_summary(w.N, P, kind),
         "ring_fwd": {"P": P, "partition": kind, "ms_overlap": round(ring_ov, 3),
                      "ms_serial": round(ring_se, 3), "ms_copies_alone": round(ring_cp, 3),
                      "tflops_overlap": round(w.flops_fwd / (ring_ov * 1e-3) / 1e12, 2),
